@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark on one node (one process per GPU).
+
+A step is one layer of one decode step for the whole batch: the new tokens'
+K/V written into their slots (plus copy-on-write block copies when the batch
+shares blocks), the per-partition decode pass, and the split-K merge.  The
+default workload is the long-context continuous batch (256 sequences, 8 at
+131072 tokens, 248 uniform in 16..32768; 64 query / 8 KV heads, head_dim 128,
+block_size 32, bf16, partitions of 512); its K/V (~21 GB) is far larger than
+L2, so no flush is needed between steps.  Smaller workloads get an L2 flush
+(a 512 MB write) between timed steps, outside the timed events.
+
+Metric: paged decode attention KV GB/s = algorithmic bytes of the decode call
+(K and V rows of every attended token, q, output, used block-table entries,
+context lengths) / step time; plus sequence-layer decode steps/s.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (there is no other reference implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-layer decode steps/s"
+L2_BYTES = 129 * 2**20
+
+
+# ------------------------------------------------------------ accounting ---
+def decode_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem, out_elem):
+    """Minimum bytes one decode call moves: K and V rows of every attended
+    token, q, the output, used block-table entries and the context lengths."""
+    lens = [int(n) for n in lens]
+    kv = sum(lens) * num_kv_heads * head_dim * 2 * kv_elem
+    qo = len(lens) * num_q_heads * head_dim * (q_elem + out_elem)
+    tables = sum(-(-n // block_size) for n in lens) * 4
+    return kv + qo + tables + 4 * len(lens)
+
+
+def partition_pass_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem):
+    """Algorithmic bytes of the per-partition pass alone: K/V rows, q, table
+    entries, lengths (its partial/output writes are not counted)."""
+    lens = [int(n) for n in lens]
+    return (sum(lens) * num_kv_heads * head_dim * 2 * kv_elem
+            + len(lens) * num_q_heads * head_dim * q_elem
+            + sum(-(-n // block_size) for n in lens) * 4 + 4 * len(lens))
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                cmd += ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ---
+def build_workload(name: str, device, seed_offset: int):
+    from paged_kv_cache_237_gb300 import engine, workloads
+    if name == "prefix_share":
+        st = engine.prefix_share_state(device, seed=workloads.WORKLOADS[name].seed + seed_offset)
+        w = st["workload"]
+        d = dict(workload=w, q=st["q"], k_cache=st["k_cache"], v_cache=st["v_cache"],
+                 block_tables=st["tables"].to(device), context_lens=st["lens"].to(device),
+                 k_new=st["k_new"], v_new=st["v_new"], slot_mapping=st["slots"].to(device),
+                 cow_pairs=st["pairs"].to(device), lens=st["lens"].numpy(), scale=st["scale"],
+                 max_context_len=st["max_context_len"])
+    else:
+        d = workloads.decode_inputs(name, device=device, seed=workloads.WORKLOADS[name].seed + seed_offset)
+        d["cow_pairs"] = None
+    return d
+
+
+def flush_l2(buf):
+    if buf is not None:
+        buf.add_(1)
+
+
+# ------------------------------------------------------------- CPU legs ---
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(d, seqs):
+    """Host copies of the blocks the sampled sequences use (gathered with torch
+    indexing on the device), ready for the oracle."""
+    bs = d["k_cache"].shape[2]
+    lens = d["lens"]
+    tab = d["block_tables"].cpu().numpy()
+    rows = [tab[s, :-(-int(lens[s]) // bs)] for s in seqs]
+    uniq = np.unique(np.concatenate(rows)) if rows else np.zeros(0, np.int64)
+    remap = {int(b): i for i, b in enumerate(uniq)}
+    idx = torch.from_numpy(uniq.astype(np.int64)).to(d["k_cache"].device)
+    kc = d["k_cache"].index_select(0, idx).cpu()
+    vc = d["v_cache"].index_select(0, idx).cpu()
+    t = np.full((len(seqs), max(1, max(len(r) for r in rows))), -1, np.int32)
+    for i, r in enumerate(rows):
+        t[i, :len(r)] = [remap[int(b)] for b in r]
+    q = d["q"][list(seqs)].cpu()
+    return q, kc, vc, torch.from_numpy(t), torch.tensor([int(lens[s]) for s in seqs], dtype=torch.int32)
+
+
+def time_oracle(d, seqs, threads):
+    import oracle
+    q, kc, vc, t, ln = oracle_sample(d, seqs)
+    t0 = time.perf_counter()
+    oracle.paged_decode(q, kc, vc, t, ln, d["scale"], threads=threads)
+    return time.perf_counter() - t0
+
+
+def pick_sample(d, target_s: float, threads: int):
+    """Sequences (seeded order, shortest first among a random draw) whose
+    oracle time is about target_s; returns (seqs, est_seconds)."""
+    lens = d["lens"]
+    rng = np.random.default_rng(1234)
+    order = [int(i) for i in rng.permutation(len(lens))]
+    probe = order[:1]
+    dt = max(time_oracle(d, probe, threads), 1e-4)
+    per_token = dt / max(1, int(lens[probe[0]]))
+    budget = target_s / per_token
+    seqs, tok = [], 0
+    for s in order:
+        if tok + int(lens[s]) > budget and seqs:
+            continue
+        seqs.append(s)
+        tok += int(lens[s])
+        if tok >= 0.9 * budget:
+            break
+    return seqs
+
+
+def sample_kv_bytes(d, seqs):
+    w = d["workload"]
+    e = torch.tensor([], dtype=w.dtype).element_size()
+    return decode_bytes([d["lens"][s] for s in seqs], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                        w.block_size, e, e, e)
+
+
+# ------------------------------------------------------------------ main ---
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_context",
+                    choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    d = build_workload(args.workload, device, seed_offset=rank)
+    w = d["workload"]
+    elem = torch.tensor([], dtype=w.dtype).element_size()
+    lens = d["lens"]
+    B = decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, elem, elem, elem)
+    B_part = partition_pass_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, elem, elem)
+    step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], d["scale"],
+                      d["max_context_len"], w.partition_size)
+    split = binding.pa_decode_workspace_size(len(lens), w.num_q_heads, w.head_dim, d["max_context_len"],
+                                             w.partition_size) > 0
+    stream = torch.cuda.current_stream(device)
+    working_set = d["k_cache"].numel() * elem * 2
+    flush = None if working_set > 2 * L2_BYTES else torch.empty(512 * 2**20 // 4, dtype=torch.float32,
+                                                                  device=device)
+    cow = d["cow_pairs"]
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        step.write_tokens(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        step.decode(stream, binding.PA_PHASE_PARTITIONS)
+        if ev is not None:
+            ev[2].record(stream)
+        step.decode(stream, binding.PA_PHASE_REDUCE)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+        flush_l2(flush)
+    torch.cuda.synchronize(device)
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+
+    K = args.steps
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.2)
+    for i in range(K):
+        one_step(events[i])
+        flush_l2(flush)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    part_ms = [e[1].elapsed_time(e[2]) for e in events]
+    red_ms = [e[2].elapsed_time(e[3]) for e in events]
+    write_ms = [e[0].elapsed_time(e[1]) for e in events]
+    ms = statistics.mean(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    launches_per_step = (1 if d["slot_mapping"].numel() else 0) + 1 + (1 if split else 0) + \
+        (1 if cow is not None and cow.numel() else 0)
+
+    # ---- end to end through the public API, host buffers in pinned memory
+    hq = d["q"].cpu().pin_memory()
+    htab = d["block_tables"].cpu().pin_memory()
+    hlen = d["context_lens"].cpu().pin_memory()
+    hk = d["k_new"].cpu().pin_memory()
+    hv = d["v_new"].cpu().pin_memory()
+    hslot = d["slot_mapping"].cpu().pin_memory()
+    hcow = cow.cpu().pin_memory() if cow is not None and cow.numel() else None
+    hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, htab, hlen, hk, hv, hslot)) + \
+        (hcow.numel() * 8 if hcow is not None else 0)
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        step.q.copy_(hq, non_blocking=True)
+        step.block_tables.copy_(htab, non_blocking=True)
+        step.context_lens.copy_(hlen, non_blocking=True)
+        d["k_new"].copy_(hk, non_blocking=True)
+        d["v_new"].copy_(hv, non_blocking=True)
+        d["slot_mapping"].copy_(hslot, non_blocking=True)
+        if hcow is not None:
+            cow.copy_(hcow, non_blocking=True)
+        step.run(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
+        hout.copy_(step.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+        flush_l2(flush)
+    torch.cuda.synchronize(device)
+    e2e_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        e2e_events[i][0].record(stream)
+        e2e_step()
+        e2e_events[i][1].record(stream)
+        flush_l2(flush)
+    torch.cuda.synchronize(device)
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_events)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- CPU baseline: the oracle as it stands, on a bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = host_cores()
+        seqs = pick_sample(d, args.cpu_seconds, threads)
+        dt = time_oracle(d, seqs, threads)
+        sb = sample_kv_bytes(d, seqs)
+        cpu = {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{len(seqs)} of {len(lens)} sequences ({int(sum(lens[s] for s in seqs))} tokens, "
+                         f"all {w.num_q_heads} query heads) of the same workload, fp64 C oracle, "
+                         f"{dt:.1f} s"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    part_avg = statistics.mean(part_ms)
+    achieved = B_part / (part_avg * 1e-3) / 1e9
+    value = world * B / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name,
+            "num_seqs": len(lens), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": w.partition_size,
+            "total_context_tokens": int(sum(int(n) for n in lens)),
+            "max_context_len": int(d["max_context_len"]),
+            "bytes_per_step": B,
+            "l2": "inputs larger than L2 (no flush)" if flush is None else "512 MB L2 flush between steps",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "hbm_fraction": round(B / (ms * 1e-3) / 1e9 / peak, 4),
+        "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
+        "phases_ms": {"cache_write": round(statistics.mean(write_ms), 4),
+                      "partition_pass": round(part_avg, 4), "split_k_reduce": round(statistics.mean(red_ms), 4)},
+        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)" if w.dtype == torch.bfloat16
+                     else "decode_f32_kernel (partition pass)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "bytes_per_launch": B_part, "traffic": None},
+        "e2e": {"value": round(world * B / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The fp64 oracle, as it stands, on the host cores: each step is a
+    bounded sample of the workload (same metric and unit)."""
+    sys.path.insert(0, ROOT)
+    from paged_kv_cache_237_gb300 import workloads
+
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    if name == "prefix_share":
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm samples only the "
+                          "decode_inputs workloads"}))
+        return
+    # Build the workload on the GPU when there is one (same generator as our arm), else on the host.
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    d = workloads.decode_inputs(name, device=device)
+    threads = host_cores()
+    per_step = max(0.5, min(10.0, 150.0 / (args.steps + args.warmup)))
+    seqs = pick_sample(d, per_step, threads)
+    sb = sample_kv_bytes(d, seqs)
+    import oracle
+    q, kc, vc, t, ln = oracle_sample(d, seqs)
+    for _ in range(args.warmup):
+        oracle.paged_decode(q, kc, vc, t, ln, d["scale"], threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, kc, vc, t, ln, d["scale"], threads=threads)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = sb / (ms * 1e-3) / 1e9
+    lens = d["lens"]
+    sample = (f"{len(seqs)} of {len(lens)} sequences ({int(sum(lens[s] for s in seqs))} tokens, all "
+              f"{w.num_q_heads} query heads) of the same workload per step, fp64 C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": len(lens), "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,864 @@
+// Paged decode attention for sm_103a.
+//
+// What is computed: for each sequence and query head, attention of the one
+// decode query over the sequence's cached K/V, which live in fixed-size
+// physical blocks reached through the sequence's block table ("PagedAttention",
+// robocikowo.com, "Jak dziala" and "Komponenty": a custom kernel reads the
+// non-contiguous cache through the block table; "PagedAttention et
+// RadixAttention : parlons de KV Cache", aitalk.it, "PagedAttention : la
+// memoire comme un systeme d'exploitation", step two).  The path is bound by
+// HBM bandwidth ("PagedAttention", robocikowo.com, "Zlozonosc obliczeniowa").
+//
+// Work decomposition.  A work item is (sequence, context partition, KV head,
+// query-head tile).  A persistent grid walks the items in order; a CTA owns an
+// item and its 4 warps split the item's 16-token chunks round-robin.  Each warp
+// runs its own ring of NSTAGE shared-memory stages, filled by TMA and tracked
+// by one mbarrier per stage, so the main loop needs no CTA-wide barrier.  At
+// the end of the item the warps' partial softmax states (max, sum, unnormalised
+// output) are merged through shared memory; single-partition sequences write
+// the final output, the others write a partial that the reduce kernel merges.
+//
+// bf16 path: each 16-token chunk of K and V arrives as 2-D TMA boxes of
+// 16 rows x 64 elements with the 128-byte swizzle, which makes the ldmatrix
+// reads below bank-conflict free.  The query-head group (up to 16 heads) is
+// the M dimension of mma.m16n8k16: S = Q K^T (tokens are N), then the fp32
+// probabilities, split into a bf16 high part and a bf16 residual, feed
+// O += P_hi V + P_lo V directly from registers (two MMAs keep ~16 bits of p).
+// fp32 path: 1-D bulk copies and SIMT fp32 FMAs, one lane per head_dim slice.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ __forceinline__ uint8_t *align_1024(uint8_t *p) {
+    uint32_t a = smem_addr(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Context length of sequence s, clamped into [0, ctx_cap].
+__device__ __forceinline__ int seq_len(const DecodeParams &p, int s) {
+    int n = p.context_lens[s];
+    return n < 0 ? 0 : (n > p.ctx_cap ? p.ctx_cap : n);
+}
+
+__device__ __forceinline__ int parts_of(int n, int P) { return n <= P ? 1 : (n + P - 1) / P; }
+
+// Position of the walk over (sequence, partition) pairs: `base` is the global
+// index of sequence `seq`'s first partition.
+struct SeqCursor {
+    int seq;
+    long long base;
+};
+
+// Move the cursor forward to the sequence that owns global partition gp
+// (32 sequences per step, warp-parallel).  False when gp is past the end.
+__device__ bool seek(SeqCursor &c, long long gp, const DecodeParams &p, int lane) {
+    while (c.seq < p.num_seqs) {
+        const int s = c.seq + lane;
+        const int np = s < p.num_seqs ? parts_of(seq_len(p, s), p.partition_size) : 0;
+        int incl = np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const unsigned hit = __ballot_sync(kFull, s < p.num_seqs && gp < c.base + incl);
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            c.base += __shfl_sync(kFull, incl - np, L);
+            c.seq += L;
+            return true;
+        }
+        c.base += __shfl_sync(kFull, incl, 31);
+        c.seq += 32;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void store4(float *dst, float4 v) { *reinterpret_cast<float4 *>(dst) = v; }
+
+__device__ __forceinline__ void store4(__nv_bfloat16 *dst, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    memcpy(&u.x, &lo, 4);
+    memcpy(&u.y, &hi, 4);
+    *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+// Merge the kWarps per-warp softmax states held in shared memory (each warp's
+// region starts with float O[16][HD + kEpiPad], then M[16], then L[16]) and
+// store either the final rows or the item's partial.
+template <typename OutT, int HD>
+__device__ void merge_and_store(const uint8_t *smem, int warp_bytes, const DecodeParams &p, int seq,
+                                int part, int qh0, int rows, bool single) {
+    constexpr int LD = HD + kEpiPad;
+    constexpr int Q4 = HD / 4;
+    for (int task = threadIdx.x; task < rows * Q4; task += blockDim.x) {
+        const int r = task / Q4, d = (task % Q4) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float *em = reinterpret_cast<const float *>(smem + w * warp_bytes) + 16 * LD;
+            M = fmaxf(M, em[r]);
+        }
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *eo = reinterpret_cast<const float *>(smem + w * warp_bytes);
+                const float f = exp2f(eo[16 * LD + r] - M);
+                L += f * eo[16 * LD + 16 + r];
+                const float4 v = *reinterpret_cast<const float4 *>(eo + r * LD + d);
+                acc.x += f * v.x;
+                acc.y += f * v.y;
+                acc.z += f * v.z;
+                acc.w += f * v.w;
+            }
+        }
+        const int qh = qh0 + r;
+        if (single) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            OutT *o = static_cast<OutT *>(p.out) + ((long long)seq * p.num_q_heads + qh) * HD + d;
+            store4(o, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        } else {
+            const long long idx = ((long long)seq * p.max_parts + part) * p.num_q_heads + qh;
+            store4(p.part_acc + idx * HD + d, acc);
+            if (d == 0) *reinterpret_cast<float2 *>(p.part_ml + idx * 2) = make_float2(M, L);
+        }
+    }
+}
+
+// Describes the item a CTA is working on.
+struct Item {
+    int seq, part, kvh, qh0, rows;
+    int tok_begin, tok_end, nchunks;
+    bool single;
+};
+
+__device__ __forceinline__ bool next_item(Item &it, SeqCursor &cur, long long item,
+                                          const DecodeParams &p, int tile_rows, int lane) {
+    const int T = p.num_kv_heads * p.head_tiles;
+    const long long gp = item / T;
+    if (!seek(cur, gp, p, lane)) return false;
+    const int r = static_cast<int>(item % T);
+    const int ht = r % p.head_tiles;
+    it.seq = cur.seq;
+    it.part = static_cast<int>(gp - cur.base);
+    it.kvh = r / p.head_tiles;
+    it.qh0 = it.kvh * p.group + ht * tile_rows;
+    it.rows = min(tile_rows, p.group - ht * tile_rows);
+    const int raw = p.context_lens[it.seq];
+    if (threadIdx.x == 0 && r == 0 && it.part == 0 && (raw < 0 || raw > p.ctx_cap))
+        flag_status(p.status, PA_STATUS_BAD_CONTEXT_LEN);
+    const int n = seq_len(p, it.seq);
+    it.tok_begin = it.part * p.partition_size;
+    it.tok_end = min(n, it.tok_begin + p.partition_size);
+    const int ntok = max(0, it.tok_end - it.tok_begin);
+    it.nchunks = (ntok + kChunk - 1) / kChunk;
+    it.single = n <= p.partition_size;
+    return true;
+}
+
+// Physical location of this warp's k-th chunk of the item, as a row of the
+// [num_blocks * Hkv * block_size, head_dim] view of a cache; an invalid block
+// id gives -1 and sets a flag (the bf16 path then loads rows past the view,
+// which TMA fills with zeros; the fp32 path skips the copy).
+__device__ __forceinline__ int chunk_row(const DecodeParams &p, const Item &it, int warp, int k) {
+    const int c = warp + kWarps * k;
+    const int tok = it.tok_begin + c * kChunk;
+    const int phys = p.block_tables[(long long)it.seq * p.max_blocks_per_seq + tok / p.block_size];
+    if (phys < 0 || phys >= p.num_blocks) {
+        flag_status(p.status, PA_STATUS_BAD_BLOCK_ID);
+        return -1;
+    }
+    return static_cast<int>(((long long)phys * p.num_kv_heads + it.kvh) * p.block_size +
+                            tok % p.block_size);
+}
+
+// ------------------------------------------------------------ bf16 path ---
+template <int HD, int NSTAGE, bool ROWS16>
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    constexpr int HALVES = HD / 64;              // 128-byte column slices per row
+    constexpr int HALF_BYTES = kChunk * 128;     // one TMA box: 16 rows x 64 bf16
+    constexpr int PAGE_BYTES = HALVES * HALF_BYTES;
+    constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K, then V
+    constexpr int WARP_BYTES = NSTAGE * STAGE_BYTES;
+    constexpr int KT = HD / 16;
+    constexpr int NT = HD / 8;
+    constexpr int LD = HD + kEpiPad;
+    static_assert(WARP_BYTES >= (16 * LD + 32) * 4, "epilogue tile must fit in a warp's stages");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t *wbuf = smem + warp * WARP_BYTES;
+    const uint32_t wbuf_s = smem_addr(wbuf);
+    const uint32_t bar_s = smem_addr(smem + kWarps * WARP_BYTES) + warp * NSTAGE * 8;
+
+    if (lane == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(bar_s + 8 * s, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncwarp();
+
+    uint32_t n_issued = 0, n_done = 0;
+    bool failed = false;
+    SeqCursor cur{0, 0};
+    const int oob_row = p.total_rows;
+
+    for (long long item = blockIdx.x;; item += gridDim.x) {
+        Item it;
+        if (!next_item(it, cur, item, p, 16, lane)) break;
+        const int my_n = it.nchunks > warp ? (it.nchunks - warp + kWarps - 1) / kWarps : 0;
+
+        // Rows of this warp's chunks: lane j holds chunks j and j + 32.
+        int rowA = oob_row, rowB = oob_row;
+        if (lane < my_n) {
+            int r = chunk_row(p, it, warp, lane);
+            rowA = r < 0 ? oob_row : r;
+        }
+        if (lane + 32 < my_n) {
+            int r = chunk_row(p, it, warp, lane + 32);
+            rowB = r < 0 ? oob_row : r;
+        }
+
+        auto issue = [&](int k) {
+            const int row = __shfl_sync(kFull, k < 32 ? rowA : rowB, k & 31);
+            if (failed) return;
+            if (lane == 0) {
+                const int s = n_issued % NSTAGE;
+                const uint32_t dst = wbuf_s + s * STAGE_BYTES, bar = bar_s + 8 * s;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    tma_load_2d(dst + h * HALF_BYTES, &tmK, h * 64, row, bar);
+                    tma_load_2d(dst + PAGE_BYTES + h * HALF_BYTES, &tmV, h * 64, row, bar);
+                }
+            }
+            ++n_issued;
+        };
+
+        // Q fragments (A operand), rows >= it.rows are zero.
+        uint32_t qa[KT][4];
+        {
+            const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q) +
+                                      ((long long)it.seq * p.num_q_heads + it.qh0) * HD;
+            const bool lo_ok = g < it.rows, hi_ok = ROWS16 && (g + 8 < it.rows);
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                const int c0 = 16 * kk + 2 * t;
+                qa[kk][0] = lo_ok ? *reinterpret_cast<const uint32_t *>(qb + g * HD + c0) : 0u;
+                qa[kk][1] = hi_ok ? *reinterpret_cast<const uint32_t *>(qb + (g + 8) * HD + c0) : 0u;
+                qa[kk][2] = lo_ok ? *reinterpret_cast<const uint32_t *>(qb + g * HD + c0 + 8) : 0u;
+                qa[kk][3] = hi_ok ? *reinterpret_cast<const uint32_t *>(qb + (g + 8) * HD + c0 + 8) : 0u;
+            }
+        }
+
+        const int pro = my_n < NSTAGE ? my_n : NSTAGE;
+        for (int k = 0; k < pro; ++k) issue(k);
+
+        float o[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+
+        for (int k = 0; k < my_n; ++k) {
+            const int s = n_done % NSTAGE;
+            const uint32_t parity = (n_done / NSTAGE) & 1u;
+            bool ok = !failed && mbar_wait_bounded(bar_s + 8 * s, parity);
+            if (__any_sync(kFull, !ok)) {
+                if (!failed && lane == 0) flag_status(p.status, PA_STATUS_WAIT_TIMEOUT);
+                failed = true;
+                break;
+            }
+            ++n_done;
+            const uint32_t Ks = wbuf_s + s * STAGE_BYTES, Vs = Ks + PAGE_BYTES;
+            const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
+            const int valid = min(kChunk, it.tok_end - tok0);
+            if (valid < kChunk) {
+                // Tokens past the context: zero their V rows so that p = 0
+                // multiplies exact zeros (the slots may hold anything, NaN too).
+                uint8_t *vg = wbuf + s * STAGE_BYTES + PAGE_BYTES;
+                const int per_half = (kChunk - valid) * 8;
+                for (int i = lane; i < HALVES * per_half; i += 32) {
+                    const int h = i / per_half, rem = i % per_half;
+                    *reinterpret_cast<uint4 *>(vg + h * HALF_BYTES + (valid + rem / 8) * 128 +
+                                               (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // S = Q K^T over the 16 tokens (two n-tiles of 8 tokens).
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3;
+                const int r = (lane & 7) + ((mi >> 1) << 3);
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    const int ch = 2 * kk + (mi & 1);
+                    const uint32_t addr =
+                        Ks + (ch >> 3) * HALF_BYTES + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = 8 * nt + 2 * t + (j & 1);
+                    sc[nt][j] = tok < valid ? sc[nt][j] * p.scale_log2 : -INFINITY;
+                }
+
+            // Online softmax, base 2.  Row g uses sc[.][0..1], row g + 8 sc[.][2..3].
+            float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(kFull, mx_lo, 1));
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(kFull, mx_lo, 2));
+            const float mn_lo = fmaxf(m_lo, mx_lo);
+            const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+            const float alpha_lo = exp2f(m_lo - ref_lo);
+            m_lo = mn_lo;
+            float alpha_hi = 1.f, ref_hi = 0.f;
+            if (ROWS16) {
+                float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(kFull, mx_hi, 1));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(kFull, mx_hi, 2));
+                const float mn_hi = fmaxf(m_hi, mx_hi);
+                ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+                alpha_hi = exp2f(m_hi - ref_hi);
+                m_hi = mn_hi;
+            }
+            // Probabilities in fp32, then split as p = hi + lo with both parts
+            // bf16, so that P V on bf16 MMAs keeps ~16 significant bits of p.
+            float pr[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                pr[nt][0] = exp2f(sc[nt][0] - ref_lo);
+                pr[nt][1] = exp2f(sc[nt][1] - ref_lo);
+                pr[nt][2] = ROWS16 ? exp2f(sc[nt][2] - ref_hi) : 0.f;
+                pr[nt][3] = ROWS16 ? exp2f(sc[nt][3] - ref_hi) : 0.f;
+            }
+            l_lo = l_lo * alpha_lo + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+            if (ROWS16) l_hi = l_hi * alpha_hi + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+            uint32_t pa[4], pb[4];
+            {
+                // A-fragment order: (row g, tok 2t..), (row g+8, tok 2t..),
+                // (row g, tok 8+2t..), (row g+8, tok 8+2t..)
+                const float *src[4][2] = {{&pr[0][0], &pr[0][1]}, {&pr[0][2], &pr[0][3]},
+                                          {&pr[1][0], &pr[1][1]}, {&pr[1][2], &pr[1][3]}};
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float x0 = *src[r4][0], x1 = *src[r4][1];
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+                    const float2 hf = __bfloat1622float2(hi);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+                    memcpy(&pa[r4], &hi, 4);
+                    memcpy(&pb[r4], &lo, 4);
+                }
+            }
+            if (__any_sync(kFull, alpha_lo != 1.f || alpha_hi != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    o[j][0] *= alpha_lo;
+                    o[j][1] *= alpha_lo;
+                    if (ROWS16) {
+                        o[j][2] *= alpha_hi;
+                        o[j][3] *= alpha_hi;
+                    }
+                }
+            }
+
+            // O += P V (k = 16 tokens, n = head_dim in tiles of 8).
+            {
+                const int mi = lane >> 3;
+                const int r = (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+                for (int jj = 0; jj < KT; ++jj) {
+                    const int ch = 2 * jj + (mi >> 1);
+                    const uint32_t addr =
+                        Vs + (ch >> 3) * HALF_BYTES + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * jj], pa, b0, b1);
+                    mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+                    mma_bf16_16816(o[2 * jj], pb, b0, b1);
+                    mma_bf16_16816(o[2 * jj + 1], pb, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (k + NSTAGE < my_n) issue(k + NSTAGE);
+        }
+
+        // Epilogue: publish this warp's state in its (now idle) stage buffers.
+        l_lo += __shfl_xor_sync(kFull, l_lo, 1);
+        l_lo += __shfl_xor_sync(kFull, l_lo, 2);
+        if (ROWS16) {
+            l_hi += __shfl_xor_sync(kFull, l_hi, 1);
+            l_hi += __shfl_xor_sync(kFull, l_hi, 2);
+        }
+        {
+            float *eo = reinterpret_cast<float *>(wbuf);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                *reinterpret_cast<float2 *>(eo + g * LD + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
+                *reinterpret_cast<float2 *>(eo + (g + 8) * LD + 8 * j + 2 * t) =
+                    ROWS16 ? make_float2(o[j][2], o[j][3]) : make_float2(0.f, 0.f);
+            }
+            if (t == 0) {
+                eo[16 * LD + g] = m_lo;
+                eo[16 * LD + 16 + g] = l_lo;
+                eo[16 * LD + g + 8] = ROWS16 ? m_hi : -INFINITY;
+                eo[16 * LD + 16 + g + 8] = ROWS16 ? l_hi : 0.f;
+            }
+        }
+        __syncthreads();
+        merge_and_store<__nv_bfloat16, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows,
+                                           it.single);
+        fence_proxy_async_smem();
+        __syncthreads();
+    }
+
+    // A wait gave up: let copies still in flight land before the CTA exits.
+    if (failed && lane == 0) {
+        for (uint32_t gi = n_done; gi < n_issued; ++gi)
+            mbar_wait_bounded(bar_s + 8 * (gi % NSTAGE), (gi / NSTAGE) & 1u);
+    }
+}
+
+// ------------------------------------------------------------ fp32 path ---
+template <int HD, int NSTAGE>
+__global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodeParams p) {
+    constexpr int VEC = HD / 32;                 // head_dim elements per lane
+    constexpr int HT = 8;                        // query heads per tile
+    constexpr int PAGE_BYTES = kChunk * HD * 4;
+    constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+    constexpr int WARP_BYTES = NSTAGE * STAGE_BYTES;
+    constexpr int LD = HD + kEpiPad;
+    static_assert(WARP_BYTES >= (16 * LD + 32) * 4, "epilogue tile must fit in a warp's stages");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *wbuf = smem + warp * WARP_BYTES;
+    const uint32_t wbuf_s = smem_addr(wbuf);
+    const uint32_t bar_s = smem_addr(smem + kWarps * WARP_BYTES) + warp * NSTAGE * 8;
+    if (lane == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(bar_s + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    uint32_t n_issued = 0, n_done = 0;
+    bool failed = false;
+    SeqCursor cur{0, 0};
+    const char *kc = static_cast<const char *>(p.k_cache);
+    const char *vc = static_cast<const char *>(p.v_cache);
+
+    for (long long item = blockIdx.x;; item += gridDim.x) {
+        Item it;
+        if (!next_item(it, cur, item, p, HT, lane)) break;
+        const int my_n = it.nchunks > warp ? (it.nchunks - warp + kWarps - 1) / kWarps : 0;
+        int rowA = -1, rowB = -1;
+        if (lane < my_n) rowA = chunk_row(p, it, warp, lane);
+        if (lane + 32 < my_n) rowB = chunk_row(p, it, warp, lane + 32);
+
+        auto issue = [&](int k) {
+            const int row = __shfl_sync(kFull, k < 32 ? rowA : rowB, k & 31);
+            if (failed) return;
+            if (lane == 0) {
+                const int s = n_issued % NSTAGE;
+                const uint32_t dst = wbuf_s + s * STAGE_BYTES, bar = bar_s + 8 * s;
+                fence_proxy_async_smem();
+                // An invalid block id completes the stage with no data (flagged).
+                mbar_arrive_expect_tx(bar, row >= 0 ? STAGE_BYTES : 0);
+                if (row >= 0) {
+                    const long long off = (long long)row * HD * 4;
+                    bulk_load(dst, kc + off, PAGE_BYTES, bar);
+                    bulk_load(dst + PAGE_BYTES, vc + off, PAGE_BYTES, bar);
+                }
+            }
+            ++n_issued;
+        };
+
+        float q[HT][VEC];
+        {
+            const float *qb = static_cast<const float *>(p.q) +
+                              ((long long)it.seq * p.num_q_heads + it.qh0) * HD + lane * VEC;
+#pragma unroll
+            for (int h = 0; h < HT; ++h)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) q[h][v] = h < it.rows ? qb[h * HD + v] : 0.f;
+        }
+        const int pro = my_n < NSTAGE ? my_n : NSTAGE;
+        for (int k = 0; k < pro; ++k) issue(k);
+
+        float acc[HT][VEC], m[HT], l[HT];
+#pragma unroll
+        for (int h = 0; h < HT; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[h][v] = 0.f;
+        }
+
+        for (int k = 0; k < my_n; ++k) {
+            const int s = n_done % NSTAGE;
+            const uint32_t parity = (n_done / NSTAGE) & 1u;
+            bool ok = !failed && mbar_wait_bounded(bar_s + 8 * s, parity);
+            if (__any_sync(kFull, !ok)) {
+                if (!failed && lane == 0) flag_status(p.status, PA_STATUS_WAIT_TIMEOUT);
+                failed = true;
+                break;
+            }
+            ++n_done;
+            const float *Ks = reinterpret_cast<const float *>(wbuf + s * STAGE_BYTES);
+            const float *Vs = Ks + kChunk * HD;
+            const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
+            const int valid = min(kChunk, it.tok_end - tok0);
+            for (int tt = 0; tt < valid; ++tt) {
+                float kv[VEC], vv[VEC];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    kv[v] = Ks[tt * HD + lane * VEC + v];
+                    vv[v] = Vs[tt * HD + lane * VEC + v];
+                }
+#pragma unroll
+                for (int h = 0; h < HT; ++h) {
+                    if (h < it.rows) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) d = fmaf(q[h][v], kv[v], d);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
+                        const float sv = d * p.scale_log2;
+                        const float mn = fmaxf(m[h], sv);
+                        const float a = exp2f(m[h] - mn);
+                        const float pr = exp2f(sv - mn);
+                        l[h] = l[h] * a + pr;
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) acc[h][v] = fmaf(acc[h][v], a, pr * vv[v]);
+                        m[h] = mn;
+                    }
+                }
+            }
+            __syncwarp();
+            if (k + NSTAGE < my_n) issue(k + NSTAGE);
+        }
+
+        {
+            float *eo = reinterpret_cast<float *>(wbuf);
+#pragma unroll
+            for (int h = 0; h < HT; ++h)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) eo[h * LD + lane * VEC + v] = acc[h][v];
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    eo[16 * LD + h] = h < HT ? m[h < HT ? h : 0] : -INFINITY;
+                    eo[16 * LD + 16 + h] = h < HT ? l[h < HT ? h : 0] : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+        merge_and_store<float, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows, it.single);
+        fence_proxy_async_smem();
+        __syncthreads();
+    }
+    if (failed && lane == 0) {
+        for (uint32_t gi = n_done; gi < n_issued; ++gi)
+            mbar_wait_bounded(bar_s + 8 * (gi % NSTAGE), (gi / NSTAGE) & 1u);
+    }
+}
+
+// ------------------------------------------------------- split-K reduce ---
+// out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p, for
+// every (sequence, query head) whose context spans more than one partition.
+// One warp per (sequence, query head); lanes own 4 consecutive head_dim values.
+template <typename OutT, int HD>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qh = blockIdx.x * 4 + warp;
+    const int seq = blockIdx.y;
+    if (qh >= p.num_q_heads) return;
+    const int n = seq_len(p, seq);
+    if (n <= p.partition_size) return;
+    const int np = (n + p.partition_size - 1) / p.partition_size;
+    const long long base = (long long)seq * p.max_parts * p.num_q_heads + qh;
+    const long long stride = p.num_q_heads;
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) M = fmaxf(M, p.part_ml[(base + i * stride) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool active = lane < HD / 4;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const long long idx = base + i * stride;
+        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + idx * 2);
+        const float f = exp2f(ml.x - M);
+        L += f * ml.y;
+        if (active) {
+            const float4 v = *reinterpret_cast<const float4 *>(p.part_acc + idx * HD + lane * 4);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+    }
+    if (active) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        OutT *o = static_cast<OutT *>(p.out) + ((long long)seq * p.num_q_heads + qh) * HD + lane * 4;
+        store4(o, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    }
+}
+
+}  // namespace pa
+
+// ================================================================ host ===
+namespace {
+
+using pa::DecodeParams;
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+int sm_count(int dev) {
+    static int cache[kMaxDevices] = {0};
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Per-kernel launch facts: dynamic smem set once, occupancy cached per device.
+struct KernelSlot {
+    int smem = 0;
+    int occupancy[kMaxDevices] = {0};
+};
+
+template <typename K>
+int ensure_kernel(K kernel, KernelSlot &slot, int smem, int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (slot.occupancy[dev] == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return 0;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, pa::kWarps * 32, smem) != cudaSuccess ||
+            occ <= 0)
+            return 0;
+        slot.smem = smem;
+        slot.occupancy[dev] = occ;
+    }
+    return slot.occupancy[dev];
+}
+
+bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(hd) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pa::kChunk)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int HD>
+constexpr int bf16_stages() { return HD == 128 ? 3 : 4; }
+template <int HD>
+constexpr int f32_stages() { return 2; }
+
+template <int HD, bool ROWS16>
+int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache, long long items,
+                int dev, cudaStream_t st) {
+    constexpr int NS = bf16_stages<HD>();
+    constexpr int STAGE = 2 * (HD / 64) * pa::kChunk * 128;
+    constexpr int SMEM = pa::kWarps * NS * STAGE + pa::kWarps * NS * 8 + 1024;
+    static KernelSlot slot;
+    auto kernel = pa::decode_bf16_kernel<HD, NS, ROWS16>;
+    const int occ = ensure_kernel(kernel, slot, SMEM, dev);
+    if (occ == 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot configure the bf16 kernel");
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, k_cache, p.total_rows, HD) || !make_map(&mv, v_cache, p.total_rows, HD))
+        return pa_fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed");
+    const long long cap = static_cast<long long>(sm_count(dev)) * occ;
+    const int grid = static_cast<int>(items < cap ? items : cap);
+    kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(mk, mv, p);
+    return PA_OK;
+}
+
+template <int HD>
+int launch_f32(const DecodeParams &p, long long items, int dev, cudaStream_t st) {
+    constexpr int NS = f32_stages<HD>();
+    constexpr int SMEM = pa::kWarps * NS * 2 * pa::kChunk * HD * 4 + pa::kWarps * NS * 8 + 1024;
+    static KernelSlot slot;
+    auto kernel = pa::decode_f32_kernel<HD, NS>;
+    const int occ = ensure_kernel(kernel, slot, SMEM, dev);
+    if (occ == 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot configure the fp32 kernel");
+    const long long cap = static_cast<long long>(sm_count(dev)) * occ;
+    const int grid = static_cast<int>(items < cap ? items : cap);
+    kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(p);
+    return PA_OK;
+}
+
+template <typename OutT, int HD>
+void launch_reduce(const DecodeParams &p, cudaStream_t st) {
+    dim3 grid((p.num_q_heads + 3) / 4, p.num_seqs);
+    pa::decode_reduce_kernel<OutT, HD><<<grid, 128, 0, st>>>(p);
+}
+
+inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int effective_partition(int partition_size) { return partition_size == 0 ? 512 : partition_size; }
+
+}  // namespace
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                           int max_context_len, int partition_size) {
+    const int P = effective_partition(partition_size);
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len <= 0 || P <= 0) return 0;
+    const long long max_parts = (max_context_len + P - 1) / P;
+    if (max_parts <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * max_parts * num_q_heads;
+    return align256(rows * 2 * sizeof(float)) + rows * head_dim * sizeof(float);
+}
+
+extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, float scale,
+                         const pa_decode_args *a) {
+    if (!a) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: args is NULL");
+    if (a->num_seqs < 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs < 0");
+    if (a->num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: null tensor pointer");
+    if (a->dtype != PA_F32 && a->dtype != PA_BF16) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: bad dtype");
+    if (a->phase < PA_PHASE_ALL || a->phase > PA_PHASE_REDUCE) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: bad phase");
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: num_q_heads must be a positive multiple of num_kv_heads");
+    if (head_dim != 64 && head_dim != 128) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim must be 64 or 128");
+    if (block_size != 16 && block_size != 32) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: block_size must be 16 or 32");
+    if (a->num_blocks <= 0 || a->max_blocks_per_seq <= 0 || a->max_context_len < 0)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: bad num_blocks, max_blocks_per_seq or max_context_len");
+    const int P = effective_partition(a->partition_size);
+    if (P < 16 || P > 4096 || P % 16 != 0)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: partition_size must be a multiple of 16 in [16, 4096]");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: out, q and caches must be 16-byte aligned");
+    const long long total_rows = static_cast<long long>(a->num_blocks) * num_kv_heads * block_size;
+    if (total_rows >= INT_MAX) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: cache has 2^31 or more rows");
+
+    const long long table_cap = static_cast<long long>(a->max_blocks_per_seq) * block_size;
+    const int ctx_cap = static_cast<int>(a->max_context_len < table_cap ? a->max_context_len : table_cap);
+    const int max_parts = ctx_cap <= P ? 1 : (ctx_cap + P - 1) / P;
+    DecodeParams p{};
+    if (max_parts > 1) {
+        const size_t need = pa_decode_workspace_size(a->num_seqs, num_q_heads, head_dim, ctx_cap, P);
+        if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace))
+            return pa_fail(PA_ERR_WORKSPACE, "pa_decode: workspace missing, unaligned or smaller than pa_decode_workspace_size()");
+        const size_t rows = static_cast<size_t>(a->num_seqs) * max_parts * num_q_heads;
+        p.part_ml = static_cast<float *>(a->workspace);
+        p.part_acc = reinterpret_cast<float *>(static_cast<char *>(a->workspace) + align256(rows * 2 * sizeof(float)));
+    }
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = a->dev_status;
+    p.num_seqs = a->num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.block_size = block_size;
+    p.num_blocks = a->num_blocks;
+    p.max_blocks_per_seq = a->max_blocks_per_seq;
+    p.partition_size = P;
+    p.max_parts = max_parts;
+    p.ctx_cap = ctx_cap;
+    p.total_rows = static_cast<int>(total_rows);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int tile = a->dtype == PA_BF16 ? 16 : 8;
+    p.tile_rows = p.group < tile ? p.group : tile;
+    p.head_tiles = (p.group + tile - 1) / tile;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return pa_fail(PA_ERR_CUDA, "pa_decode: no CUDA device");
+    if (sm_count(dev) <= 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot query the SM count");
+    cudaStream_t st = static_cast<cudaStream_t>(a->stream);
+    const long long items = static_cast<long long>(a->num_seqs) * max_parts * num_kv_heads * p.head_tiles;
+
+    int rc = PA_OK;
+    if (a->phase == PA_PHASE_REDUCE) {
+        // only the merge pass below
+    } else if (a->dtype == PA_BF16) {
+        const bool rows16 = p.group > 8;
+        if (head_dim == 128)
+            rc = rows16 ? launch_bf16<128, true>(p, k_cache, v_cache, items, dev, st)
+                        : launch_bf16<128, false>(p, k_cache, v_cache, items, dev, st);
+        else
+            rc = rows16 ? launch_bf16<64, true>(p, k_cache, v_cache, items, dev, st)
+                        : launch_bf16<64, false>(p, k_cache, v_cache, items, dev, st);
+    } else {
+        rc = head_dim == 128 ? launch_f32<128>(p, items, dev, st) : launch_f32<64>(p, items, dev, st);
+    }
+    if (rc != PA_OK) return rc;
+    if (max_parts > 1 && a->phase != PA_PHASE_PARTITIONS) {
+        if (a->dtype == PA_BF16) {
+            if (head_dim == 128) launch_reduce<__nv_bfloat16, 128>(p, st);
+            else launch_reduce<__nv_bfloat16, 64>(p, st);
+        } else {
+            if (head_dim == 128) launch_reduce<float, 128>(p, st);
+            else launch_reduce<float, 64>(p, st);
+        }
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
+    return PA_OK;
+}

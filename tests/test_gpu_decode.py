@@ -1,0 +1,138 @@
+"""pa_decode on the GPU against the fp64 oracle: edge cases, group sizes,
+head dims, block sizes, split-K partitioning, NaN tails, status flags,
+determinism and placement invariance."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_decode_close, make_case, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100, 511, 512, 513, 1000, 2049]
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_cache_237_gb300 import binding
+    return binding
+
+
+def run(pa, q, kc, vc, tables, lens, scale, partition_size=0, status=None, max_ctx=None):
+    out = torch.empty_like(q)
+    max_ctx = int(lens.max().item()) if max_ctx is None else max_ctx
+    pa.pa_decode(out, q, kc, vc, tables, lens, scale, max_context_len=max_ctx,
+                 partition_size=partition_size, status=status)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (16, 2), (16, 1), (12, 4), (40, 2)])
+def test_edge_lengths_match_oracle(pa, dtype, hd, bs, Hq, Hkv):
+    q, kc, vc, tables, lens = make_case(EDGE_LENS, Hq, Hkv, hd, bs, dtype, seed=hd + bs + Hq)
+    scale = 1.0 / math.sqrt(hd)
+    status = pa.DeviceStatus()
+    out = run(pa, q, kc, vc, tables, lens, scale, status=status)
+    assert status.read() == 0
+    ref = oracle_decode(q, kc, vc, tables, lens, scale)
+    assert_decode_close(out, ref, dtype, what=f"{dtype} hd{hd} bs{bs} {Hq}/{Hkv}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("P", [16, 64, 512, 4096])
+def test_partition_sizes_match_oracle(pa, dtype, P):
+    lens = [1, 16, 17, 64, 65, 700, 4096, 5000]
+    q, kc, vc, tables, lens_t = make_case(lens, 8, 1, 128, 16, dtype, seed=P)
+    out = run(pa, q, kc, vc, tables, lens_t, 0.088, partition_size=P)
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 0.088)
+    assert_decode_close(out, ref, dtype, what=f"P={P}")
+
+
+def test_split_and_unsplit_agree(pa):
+    lens = [3000, 4096, 77]
+    q, kc, vc, tables, lens_t = make_case(lens, 8, 2, 128, 32, torch.bfloat16, seed=3)
+    a = run(pa, q, kc, vc, tables, lens_t, 0.1, partition_size=128).double()
+    b = run(pa, q, kc, vc, tables, lens_t, 0.1, partition_size=4096).double()
+    assert_decode_close(a, b, torch.bfloat16, what="split vs unsplit")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_empty_context_and_zero_scale(pa, dtype):
+    lens = [0, 5, 40, 0]
+    q, kc, vc, tables, lens_t = make_case(lens, 4, 2, 64, 16, dtype, seed=9)
+    out = run(pa, q, kc, vc, tables, lens_t, 0.125, max_ctx=64)
+    assert torch.equal(out[0].float().cpu(), torch.zeros(4, 64))
+    assert torch.equal(out[3].float().cpu(), torch.zeros(4, 64))
+    out0 = run(pa, q, kc, vc, tables, lens_t, 0.0)
+    ref0 = oracle_decode(q, kc, vc, tables, lens_t, 0.0)
+    assert_decode_close(out0, ref0, dtype, what="scale 0")
+
+
+def test_single_token_returns_value_row(pa):
+    q, kc, vc, tables, lens = make_case([1, 1, 1], 8, 8, 128, 16, torch.float32, seed=2)
+    out = run(pa, q, kc, vc, tables, lens, 0.3)
+    for s in range(3):
+        v0 = vc[tables[s, 0].long(), :, 0, :]
+        assert torch.allclose(out[s], v0, rtol=0, atol=1e-6)
+
+
+def test_outputs_are_deterministic_and_placement_invariant(pa):
+    lens = [700, 1500, 33, 2048]
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=4, nan_tails=False)
+    a = run(pa, q, kc, vc, tables, lens_t, 0.1)
+    b = run(pa, q, kc, vc, tables, lens_t, 0.1)
+    assert torch.equal(a, b)
+    # move every block to a new physical id and rewrite the tables
+    nb = kc.shape[0]
+    perm = torch.from_numpy(np.random.default_rng(8).permutation(nb)).cuda()
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    t2 = torch.where(tables >= 0, perm[tables.clamp(min=0).long()].int(), tables)
+    c = run(pa, q, kc2, vc2, t2, lens_t, 0.1)
+    assert torch.equal(a, c)
+
+
+def test_bad_block_id_and_length_are_flagged_not_faulted(pa):
+    lens = [40, 40, 40]
+    q, kc, vc, tables, lens_t = make_case(lens, 8, 2, 128, 16, torch.bfloat16, seed=5)
+    good = run(pa, q, kc, vc, tables, lens_t, 0.1)
+    bad = tables.clone()
+    bad[1, 1] = kc.shape[0] + 1000          # outside the pool
+    bad[2, 0] = -5
+    status = pa.DeviceStatus()
+    out = run(pa, q, kc, vc, bad, lens_t, 0.1, status=status)
+    assert status.read() & pa.STATUS_BAD_BLOCK_ID
+    assert torch.equal(out[0], good[0])
+    long_lens = lens_t.clone()
+    long_lens[0] = 10_000                   # beyond the 3-entry table row
+    out = run(pa, q, kc, vc, tables, long_lens, 0.1, status=status, max_ctx=10_000)
+    assert status.read() & pa.STATUS_BAD_CONTEXT_LEN
+    assert torch.equal(out[1], good[1])
+
+
+def test_bad_block_id_fp32_path_is_flagged(pa):
+    q, kc, vc, tables, lens_t = make_case([20, 20], 4, 4, 64, 16, torch.float32, seed=6)
+    bad = tables.clone()
+    bad[0, 1] = 1 << 20
+    status = pa.DeviceStatus()
+    out = run(pa, q, kc, vc, bad, lens_t, 0.1, status=status)
+    assert status.read() & pa.STATUS_BAD_BLOCK_ID
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 0.1)
+    assert_decode_close(out[1:], ref[1:], torch.float32)
+
+
+def test_large_batch_many_items(pa):
+    """More work items than one persistent wave, mixed lengths, GQA 8."""
+    rng = np.random.default_rng(12)
+    lens = rng.integers(1, 3000, size=96).tolist()
+    q, kc, vc, tables, lens_t = make_case(lens, 32, 4, 128, 16, torch.bfloat16, seed=12)
+    out = run(pa, q, kc, vc, tables, lens_t, 1 / math.sqrt(128), partition_size=256)
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 1 / math.sqrt(128))
+    assert_decode_close(out, ref, torch.bfloat16, what="96 seqs")

@@ -1,0 +1,109 @@
+"""The five synthetic workloads, run as one decode step on the GPU and
+compared with the fp64 oracle: whole outputs for the four that the oracle
+finishes in seconds, sampled sequences (all heads) at full size for the
+long-context batch, in the same launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_decode_close, compact_for_oracle, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_cache_237_gb300 import binding, engine, workloads
+    return binding, engine, workloads
+
+
+def bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def step_and_check(pa, name, full=True):
+    binding, engine, workloads = pa
+    d = workloads.decode_inputs(name, device="cuda")
+    w = d["workload"]
+    step = engine.DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                             d["scale"], d["max_context_len"], w.partition_size)
+    kc_before = d["k_cache"].cpu() if full else None
+    vc_before = d["v_cache"].cpu() if full else None
+    out = step.run(d["k_new"], d["v_new"], d["slot_mapping"])
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    return d, step, out, kc_before, vc_before
+
+
+def test_tiny_f32_step(pa):
+    d, step, out, kc0, vc0 = step_and_check(pa, "tiny_f32")
+    # cache writes: bit-exact against the oracle's host write
+    oracle.reshape_and_cache(d["k_new"].cpu(), d["v_new"].cpu(), kc0, vc0, d["slot_mapping"].cpu())
+    assert torch.equal(bits(d["k_cache"].cpu()), bits(kc0))
+    assert torch.equal(bits(d["v_cache"].cpu()), bits(vc0))
+    ref = oracle_decode(d["q"], kc0, vc0, d["block_tables"], d["context_lens"], d["scale"])
+    assert_decode_close(out, ref, torch.float32, what="tiny_f32")
+
+
+@pytest.mark.parametrize("name", ["mha_llama2_7b", "gqa_llama3_70b"])
+def test_bf16_workload_step_full_parity(pa, name):
+    d, step, out, kc0, vc0 = step_and_check(pa, name)
+    oracle.reshape_and_cache(d["k_new"].cpu(), d["v_new"].cpu(), kc0, vc0, d["slot_mapping"].cpu())
+    assert torch.equal(bits(d["k_cache"].cpu()), bits(kc0))
+    ref = oracle_decode(d["q"], kc0, vc0, d["block_tables"], d["context_lens"], d["scale"])
+    assert_decode_close(out, ref, torch.bfloat16, what=name)
+
+
+def test_prefix_share_step_with_copy_on_write(pa):
+    binding, engine, _ = pa
+    st = engine.prefix_share_state("cuda")
+    bm = st["block_manager"]
+    assert all(bm.refcount(b) == 50 for b in st["prompt_blocks"])
+    pairs = st["pairs"]
+    suffix = st["lens"].numpy()[0::2] - 2049      # pair suffix length u
+    assert len(pairs) == int(np.count_nonzero(suffix % 16)), "one copy per pair with a partial last block"
+    kc0, vc0 = st["k_cache"].cpu(), st["v_cache"].cpu()
+    tables = st["tables"].cuda()
+    lens = st["lens"].cuda()
+    step = engine.DecodeStep(st["q"], st["k_cache"], st["v_cache"], tables, lens, st["scale"],
+                             st["max_context_len"])
+    out = step.run(st["k_new"], st["v_new"], st["slots"].cuda(), st["pairs"].cuda())
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    oracle.copy_blocks(kc0, vc0, pairs)
+    oracle.reshape_and_cache(st["k_new"].cpu(), st["v_new"].cpu(), kc0, vc0, st["slots"])
+    assert torch.equal(bits(st["k_cache"].cpu()), bits(kc0))
+    assert torch.equal(bits(st["v_cache"].cpu()), bits(vc0))
+    ref = oracle_decode(st["q"], kc0, vc0, st["tables"], st["lens"], st["scale"])
+    assert_decode_close(out, ref, torch.bfloat16, what="prefix_share")
+
+
+def test_long_context_full_size_sampled(pa):
+    """Full 256-sequence batch (8 x 131072 + 248 mixed), bs 32, partitions of
+    512; the oracle checks every head of 10 sampled sequences, including two
+    of the 131072-token ones and the shortest one."""
+    binding, engine, workloads = pa
+    d = workloads.decode_inputs("long_context", device="cuda")
+    w = d["workload"]
+    step = engine.DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                             d["scale"], d["max_context_len"], w.partition_size)
+    out = step.run(d["k_new"], d["v_new"], d["slot_mapping"])
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    lens = d["lens"]
+    longs = [int(i) for i in np.flatnonzero(lens == 131072)[:2]]
+    rng = np.random.default_rng(0)
+    others = [int(i) for i in rng.choice(np.flatnonzero(lens < 131072), size=7, replace=False)]
+    seqs = sorted(set(longs + others + [int(np.argmin(lens))]))
+    kc, vc, tab, ln = compact_for_oracle(d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"], seqs)
+    ref = oracle.paged_decode(d["q"][seqs].cpu(), kc, vc, tab, ln, d["scale"])
+    assert_decode_close(out[seqs], ref, torch.bfloat16, what="long_context sample")
+    # the step's cache writes landed: each sampled sequence's last token row equals k_new
+    for s in seqs:
+        slot = int(d["slot_mapping"][s])
+        row = d["k_cache"][slot // w.block_size, :, slot % w.block_size, :]
+        assert torch.equal(bits(row.cpu()), bits(d["k_new"][s].cpu()))
+    del d, step, out
+    torch.cuda.empty_cache()
