@@ -126,6 +126,34 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                 int max_context_len, int partition_size);
 
+/* ---- decode attention without a caller workspace ----------------------
+ * The paper has no counterpart to this call; it is a convenience of this
+ * library.
+ *
+ * For callers that cannot allocate device memory -- a plugin or framework
+ * that owns every allocation and passes the library only its inputs and
+ * outputs, or a hot path where a cudaMalloc, which may synchronise the
+ * device, is not allowed.  Same computation, arguments and results as
+ * pa_decode; args->workspace and args->workspace_bytes are ignored.  The
+ * split-K scratch is a fixed array of PA_NOALLOC_WORKSPACE_BYTES (64 MiB)
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  The call allocates and frees nothing.
+ *  - Sizes whose pa_decode_workspace_size() exceeds PA_NOALLOC_WORKSPACE_BYTES
+ *    are rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device that needs the scratch looks up its device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture on the device.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents; no part of it needs to start at zero (each call writes every
+ *    partial it reads).  Calls that overlap on the GPU -- on different streams
+ *    without ordering between them -- race on the array. */
+#define PA_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      float scale, const pa_decode_args *args);
+
 /* ---- cache write ------------------------------------------------------
  * [P3] "Jak dziala" and [P4] step three: blocks are filled as the sequence
  * grows.  For each token t with slot s = slot_mapping[t] >= 0:

@@ -68,6 +68,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     lib.pa_decode.restype = i32
     lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.POINTER(_DecodeArgs)]
+    lib.pa_decode_noalloc.restype = i32
+    lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                      ctypes.POINTER(_DecodeArgs)]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_reshape_and_cache.restype = i32

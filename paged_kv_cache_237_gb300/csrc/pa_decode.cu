@@ -862,3 +862,69 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
     return PA_OK;
 }
+
+// ====================================================== no-alloc variant ===
+// Some callers cannot allocate device memory for the split-K workspace: a
+// plugin or host framework that owns every device allocation and hands the
+// library only its input and output tensors, or a latency-critical path where
+// a cudaMalloc (which may synchronise the device) is not allowed.  For them the
+// entry point below runs the same decode with its scratch in a fixed array
+// that lives in this library's device image.  The array is sized to
+// PA_NOALLOC_WORKSPACE_BYTES and, like any __device__ variable, is held on
+// every GPU that loads the library until the process exits.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_WORKSPACE_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch per device.  In host code the symbol is
+// only a host-side handle, never a device address, so it is resolved with
+// cudaGetSymbolAddress once per device, with that device current.
+void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mutex;
+
+int noalloc_scratch(int dev, void **ptr) {
+    if (dev < 0 || dev >= kMaxDevices) return pa_fail(PA_ERR_CUDA, "pa_decode_noalloc: device index out of range");
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return pa_fail(PA_ERR_CUDA, "pa_decode_noalloc: cudaGetSymbolAddress of the static scratch failed");
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, float scale,
+                                 const pa_decode_args *args) {
+    if (!args) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode_noalloc: args is NULL");
+    if (args->num_seqs == 0) return PA_OK;
+    const int P = effective_partition(args->partition_size);
+    const long long table_cap = static_cast<long long>(args->max_blocks_per_seq) * block_size;
+    const int ctx_cap = static_cast<int>(args->max_context_len < table_cap ? args->max_context_len : table_cap);
+    const size_t need = pa_decode_workspace_size(args->num_seqs, num_q_heads, head_dim, ctx_cap, P);
+    if (need > PA_NOALLOC_WORKSPACE_BYTES)
+        return pa_fail(PA_ERR_WORKSPACE,
+                       "pa_decode_noalloc: these sizes need more split-K scratch than the library's fixed "
+                       "PA_NOALLOC_WORKSPACE_BYTES; use pa_decode with a caller workspace");
+    pa_decode_args a = *args;
+    a.workspace = nullptr;
+    a.workspace_bytes = 0;
+    if (need > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return pa_fail(PA_ERR_CUDA, "pa_decode_noalloc: no CUDA device");
+        void *scratch = nullptr;
+        int rc = noalloc_scratch(dev, &scratch);
+        if (rc != PA_OK) return rc;
+        a.workspace = scratch;
+        a.workspace_bytes = PA_NOALLOC_WORKSPACE_BYTES;
+    }
+    return pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, &a);
+}
