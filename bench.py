@@ -38,6 +38,28 @@ import torch  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-layer decode steps/s"
 L2_BYTES = 129 * 2**20
 
+# DRAM read+write bytes of one partition-pass launch from a single ncu capture
+# (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
+# batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
+# attended tokens.  Valid only while the kernel source is the one captured.
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "18f3cec118add56b", "bytes": 918.15e6, "tokens": 219876,
+                   "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
+
+
+def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype: str):
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc", "pa_decode.cu")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    c = TRAFFIC_CAPTURE
+    if (digest != c["source_sha256_prefix"] or num_kv_heads != c["num_kv_heads"] or head_dim != c["head_dim"]
+            or dtype != c["dtype"]):
+        return None
+    return int(c["bytes"] * total_tokens / c["tokens"])
+
 
 # ------------------------------------------------------------ accounting ---
 def decode_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem, out_elem):
@@ -392,7 +414,9 @@ def main():
                      else "decode_f32_kernel (partition pass)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "bytes_per_launch": B_part, "traffic": None},
+                     "bytes_per_launch": B_part,
+                     "traffic": captured_traffic(int(sum(int(n) for n in lens)), w.num_kv_heads, w.head_dim,
+                                                 "bf16" if w.dtype == torch.bfloat16 else "f32")},
         "e2e": {"value": round(world * B / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
