@@ -147,6 +147,18 @@ def build_workload(name: str, device, seed_offset: int):
     return d
 
 
+def combine_ranks(ms_local: float, bytes_local: int, dist=None, device="cpu"):
+    """Step time and bytes for the whole job: the slowest rank's time (MAX)
+    and every rank's bytes (SUM).  Without a process group, the local values."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms_local, bytes_local
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    b = torch.tensor([float(bytes_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
 def flush_l2(buf):
     if buf is not None:
         buf.add_(1)
@@ -305,11 +317,7 @@ def main():
     part_ms = [e[1].elapsed_time(e[2]) for e in events]
     red_ms = [e[2].elapsed_time(e[3]) for e in events]
     write_ms = [e[0].elapsed_time(e[1]) for e in events]
-    ms = statistics.mean(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, B_job = combine_ranks(statistics.mean(step_ms), B, dist, device)
     launches_per_step = (1 if d["slot_mapping"].numel() else 0) + 1 + (1 if split else 0) + \
         (1 if cow is not None and cow.numel() else 0)
 
@@ -349,11 +357,7 @@ def main():
         e2e_events[i][1].record(stream)
         flush_l2(flush)
     torch.cuda.synchronize(device)
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_events)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, _ = combine_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_events), B, dist, device)
 
     # ---- CPU baseline: the oracle as it stands, on a bounded sample
     cpu = None
@@ -382,7 +386,7 @@ def main():
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     part_avg = statistics.mean(part_ms)
     achieved = B_part / (part_avg * 1e-3) / 1e9
-    value = world * B / (ms * 1e-3) / 1e9
+    value = B_job / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -417,7 +421,7 @@ def main():
                      "bytes_per_launch": B_part,
                      "traffic": captured_traffic(int(sum(int(n) for n in lens)), w.num_kv_heads, w.head_dim,
                                                  "bf16" if w.dtype == torch.bfloat16 else "f32")},
-        "e2e": {"value": round(world * B / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(B_job / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
         "clocks": clk,
