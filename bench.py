@@ -42,8 +42,15 @@ L2_BYTES = 129 * 2**20
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
 # batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
 # attended tokens.  Valid only while the kernel source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "18f3cec118add56b", "bytes": 918.15e6, "tokens": 219876,
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "500ab37f20fe44ad", "bytes": 918.15e6, "tokens": 219876,
                    "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
+
+
+def kernel_source(text: bytes) -> bytes:
+    """The part of pa_decode.cu that the partition pass is compiled from: the
+    includes, device helpers and the bf16/fp32 kernels, up to the reduce kernel."""
+    cut = text.find(b"// ------------------------------------------------------- split-K reduce ---")
+    return text if cut < 0 else text[:cut]
 
 
 def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype: str):
@@ -51,7 +58,7 @@ def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype:
     src = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc", "pa_decode.cu")
     try:
         with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+            digest = hashlib.sha256(kernel_source(f.read())).hexdigest()[:16]
     except OSError:
         return None
     c = TRAFFIC_CAPTURE

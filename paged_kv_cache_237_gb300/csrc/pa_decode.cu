@@ -592,27 +592,40 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
 // ------------------------------------------------------- split-K reduce ---
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p, for
 // every (sequence, query head) whose context spans more than one partition.
-// One warp per (sequence, query head); lanes own 4 consecutive head_dim values.
+// One CTA per (query head, sequence): the threads first take M over all
+// partitions, then each warp sums a strided subset of the partitions (lanes own
+// 4 consecutive head_dim values) and the warps' sums are added in shared memory.
+constexpr int kReduceWarps = 8;
+
 template <typename OutT, int HD>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qh = blockIdx.x * 4 + warp;
+    const int qh = blockIdx.x;
     const int seq = blockIdx.y;
-    if (qh >= p.num_q_heads) return;
     const int n = seq_len(p, seq);
     if (n <= p.partition_size) return;
     const int np = (n + p.partition_size - 1) / p.partition_size;
     const long long base = (long long)seq * p.max_parts * p.num_q_heads + qh;
     const long long stride = p.num_q_heads;
+    __shared__ float s_max[kReduceWarps];
+    __shared__ float s_l[kReduceWarps];
+    __shared__ float4 s_acc[kReduceWarps][HD / 4];
+
     float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) M = fmaxf(M, p.part_ml[(base + i * stride) * 2]);
+    for (int i = threadIdx.x; i < np; i += blockDim.x) M = fmaxf(M, p.part_ml[(base + i * stride) * 2]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0) s_max[warp] = M;
+    __syncthreads();
+    M = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kReduceWarps; ++w) M = fmaxf(M, s_max[w]);
+
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool active = lane < HD / 4;
 #pragma unroll 4
-    for (int i = 0; i < np; ++i) {
+    for (int i = warp; i < np; i += kReduceWarps) {
         const long long idx = base + i * stride;
         const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + idx * 2);
         const float f = exp2f(ml.x - M);
@@ -625,10 +638,24 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
             acc.w += f * v.w;
         }
     }
-    if (active) {
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (active) s_acc[warp][lane] = acc;
+    if (lane == 0) s_l[warp] = L;
+    __syncthreads();
+    if (warp == 0 && active) {
+        float Lt = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            Lt += s_l[w];
+            const float4 v = s_acc[w][lane];
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
         OutT *o = static_cast<OutT *>(p.out) + ((long long)seq * p.num_q_heads + qh) * HD + lane * 4;
-        store4(o, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        store4(o, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
     }
 }
 
@@ -746,8 +773,8 @@ int launch_f32(const DecodeParams &p, long long items, int dev, cudaStream_t st)
 
 template <typename OutT, int HD>
 void launch_reduce(const DecodeParams &p, cudaStream_t st) {
-    dim3 grid((p.num_q_heads + 3) / 4, p.num_seqs);
-    pa::decode_reduce_kernel<OutT, HD><<<grid, 128, 0, st>>>(p);
+    dim3 grid(p.num_q_heads, p.num_seqs);
+    pa::decode_reduce_kernel<OutT, HD><<<grid, pa::kReduceWarps * 32, 0, st>>>(p);
 }
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
