@@ -245,8 +245,14 @@ def main():
                     choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--study", choices=["placement"], default=None,
+                    help="instead of the benchmark line, print one study line: 'placement' times the partition "
+                         "pass with shuffled vs identity block placement at block sizes 32 and 16")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.study == "placement":
+        run_placement_study(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -437,6 +443,58 @@ def main():
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def time_partition_pass(d, steps: int, warmup: int) -> float:
+    """Mean CUDA-event time (ms) of the per-partition decode pass alone."""
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    w = d["workload"]
+    step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], d["scale"],
+                      d["max_context_len"], w.partition_size)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.decode(stream, binding.PA_PHASE_PARTITIONS)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        step.decode(stream, binding.PA_PHASE_PARTITIONS)
+        b.record(stream)
+    torch.cuda.synchronize()
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def run_placement_study(args):
+    """Gather overhead and block-size trade-off on the same kernel: the
+    partition pass over the long-context lengths with every sequence's blocks
+    shuffled across the pool or laid out consecutively, at block size 32 and 16."""
+    from paged_kv_cache_237_gb300 import build as pa_build
+    from paged_kv_cache_237_gb300 import workloads
+    pa_build.build()
+    torch.cuda.set_device(0)
+    name = args.workload
+    rows = {}
+    for bs in (32, 16):
+        for shuffle in (True, False):
+            d = workloads.decode_inputs(name, device="cuda", shuffle=shuffle, block_size=bs)
+            w = d["workload"]
+            e = torch.tensor([], dtype=w.dtype).element_size()
+            B = partition_pass_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, bs, e, e)
+            ms = time_partition_pass(d, args.steps, args.warmup)
+            rows[f"bs{bs}_{'shuffled' if shuffle else 'identity'}"] = {
+                "ms": round(ms, 4), "GBps": round(B / (ms * 1e-3) / 1e9, 1),
+                "table_entries": int(sum(-(-int(n) // bs) for n in d["lens"]))}
+            del d
+            torch.cuda.empty_cache()
+    out = {"study": "placement", "workload": name, "steps": args.steps, "kernel": "partition pass",
+           "results": rows,
+           "gather_overhead_bs32": round(rows["bs32_shuffled"]["ms"] / rows["bs32_identity"]["ms"] - 1, 4),
+           "gather_overhead_bs16": round(rows["bs16_shuffled"]["ms"] / rows["bs16_identity"]["ms"] - 1, 4),
+           "bs16_vs_bs32_shuffled": round(rows["bs16_shuffled"]["ms"] / rows["bs32_shuffled"]["ms"] - 1, 4)}
+    print(json.dumps(out), flush=True)
 
 
 def run_reference(args):

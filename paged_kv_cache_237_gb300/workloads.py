@@ -146,15 +146,21 @@ def new_token_slots(lens: np.ndarray, tables: np.ndarray, block_size: int) -> np
 
 
 def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: bool = True,
-                  lens_override=None) -> dict:
+                  lens_override=None, block_size: int | None = None) -> dict:
     """All inputs of one decode step of a workload (except prefix_share).
 
     Returns a dict with q [S, Hq, hd], k_cache/v_cache [num_blocks, Hkv, bs, hd],
     block_tables [S, max_blocks] int32, context_lens [S] int32, k_new/v_new
     [T, Hkv, hd] and slot_mapping [T] int64 (the step's cache writes), plus the
-    workload record and host copies of lengths and tables.
+    workload record and host copies of lengths and tables.  ``shuffle=False``
+    places every sequence's blocks consecutively (identity placement);
+    ``block_size`` overrides the workload's block size (same lengths, same
+    pool fill).
     """
     w = WORKLOADS[name]
+    if block_size is not None and block_size != w.block_size:
+        w = Workload(w.name, w.dtype, w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, block_size,
+                     w.partition_size, w.seed, w.notes, w.extra)
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     lens = context_lengths(w, rng) if lens_override is None else np.asarray(lens_override, np.int64)
