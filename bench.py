@@ -245,6 +245,9 @@ def main():
                     choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="write the new tokens with a separate pa_reshape_and_cache launch instead of inside "
+                         "the decode launch")
     ap.add_argument("--study", choices=["placement"], default=None,
                     help="instead of the benchmark line, print one study line: 'placement' times the partition "
                          "pass with shuffled vs identity block placement at block sizes 32 and 16")
@@ -292,13 +295,25 @@ def main():
                                                                   device=device)
     cow = d["cow_pairs"]
 
+    # The fused launch writes each sequence's last position; a workload whose
+    # writes go elsewhere (the tiny fp32 case writes 4 random slots) runs unfused.
+    from paged_kv_cache_237_gb300.workloads import new_token_slots
+    last_slots = new_token_slots(lens, d["block_tables"].cpu().numpy(), w.block_size)
+    fused = (not args.unfused and d["slot_mapping"].numel() == len(lens)
+             and bool(np.array_equal(last_slots, d["slot_mapping"].cpu().numpy())))
+    new_tok = (d["k_new"], d["v_new"], d["slot_mapping"]) if fused else (None, None, None)
+
     def one_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        step.write_tokens(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
+        if fused:
+            if cow is not None and cow.numel():
+                binding.pa_copy_blocks(step.k_cache, step.v_cache, cow, status=step.status, stream=stream)
+        else:
+            step.write_tokens(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
         if ev is not None:
             ev[1].record(stream)
-        step.decode(stream, binding.PA_PHASE_PARTITIONS)
+        step.decode(stream, binding.PA_PHASE_PARTITIONS, *new_tok)
         if ev is not None:
             ev[2].record(stream)
         step.decode(stream, binding.PA_PHASE_REDUCE)
@@ -331,7 +346,7 @@ def main():
     red_ms = [e[2].elapsed_time(e[3]) for e in events]
     write_ms = [e[0].elapsed_time(e[1]) for e in events]
     ms, B_job = combine_ranks(statistics.mean(step_ms), B, dist, device)
-    launches_per_step = (1 if d["slot_mapping"].numel() else 0) + 1 + (1 if split else 0) + \
+    launches_per_step = (0 if fused or not d["slot_mapping"].numel() else 1) + 1 + (1 if split else 0) + \
         (1 if cow is not None and cow.numel() else 0)
 
     # ---- end to end through the public API, host buffers in pinned memory
@@ -356,7 +371,10 @@ def main():
         d["slot_mapping"].copy_(hslot, non_blocking=True)
         if hcow is not None:
             cow.copy_(hcow, non_blocking=True)
-        step.run(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
+        if fused:
+            step.run_fused(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
+        else:
+            step.run(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
         hout.copy_(step.out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -425,7 +443,9 @@ def main():
         },
         "hbm_fraction": round(B / (ms * 1e-3) / 1e9 / peak, 4),
         "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
-        "phases_ms": {"cache_write": round(statistics.mean(write_ms), 4),
+        "step": "copy-on-write copies + decode launch that also writes the new tokens + split-K merge" if fused
+                else "copy-on-write copies + cache write + decode + split-K merge",
+        "phases_ms": {"cache_updates": round(statistics.mean(write_ms), 4),
                       "partition_pass": round(part_avg, 4), "split_k_reduce": round(statistics.mean(red_ms), 4)},
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)" if w.dtype == torch.bfloat16
                      else "decode_f32_kernel (partition pass)",

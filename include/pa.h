@@ -108,6 +108,18 @@ typedef struct pa_decode_args {
                                the partials; it must follow phase 1 on the same
                                stream with identical arguments.  Splitting lets a
                                caller time or overlap the two passes. */
+    /* Optional fused cache write (all three NULL to disable).  Sequence i's new
+     * token is its last one, position context_lens[i] - 1: the call writes
+     * k_new[i] / v_new[i] ([num_seqs][num_kv_heads][head_dim], dtype) into
+     * k_cache / v_cache at slot_mapping[i] and attends with those values, the
+     * same result as pa_reshape_and_cache followed by pa_decode, in one launch
+     * fewer.  slot_mapping[i] < 0 skips sequence i's write.  A slot that is not
+     * the slot of position context_lens[i] - 1 is not written and sets
+     * PA_STATUS_BAD_SLOT.  When enabled, k_cache and v_cache are written.
+     * (Pages: [P3] "Jak dziala", [P4] step three.) */
+    const void *k_new;
+    const void *v_new;
+    const int64_t *slot_mapping;
 } pa_decode_args;
 
 #define PA_PHASE_ALL 0

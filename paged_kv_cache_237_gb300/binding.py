@@ -57,6 +57,9 @@ class _DecodeArgs(ctypes.Structure):
         ("dev_status", ctypes.c_void_p),
         ("stream", ctypes.c_void_p),
         ("phase", ctypes.c_int),
+        ("k_new", ctypes.c_void_p),
+        ("v_new", ctypes.c_void_p),
+        ("slot_mapping", ctypes.c_void_p),
     ]
 
 
@@ -185,7 +188,9 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max
 def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *,
               max_context_len: int, partition_size: int = 0, workspace: torch.Tensor | None = None,
-              status: DeviceStatus | None = None, stream=None, phase: int = 0) -> torch.Tensor:
+              status: DeviceStatus | None = None, stream=None, phase: int = 0,
+              k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+              slot_mapping: torch.Tensor | None = None) -> torch.Tensor:
     """Paged decode attention; writes ``out`` [S, Hq, hd] and returns it.
 
     q [S, Hq, hd]; k_cache, v_cache [num_blocks, Hkv, block_size, hd];
@@ -193,6 +198,10 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     sequence may span more than one partition a workspace of
     ``pa_decode_workspace_size`` bytes is needed; if none is given one is
     allocated with torch for this call.
+
+    With k_new, v_new [S, Hkv, hd] and slot_mapping [S] int64, each
+    sequence's new (last) token is written into the caches and attended in the
+    same launch (fused cache write).
     """
     fdt = (torch.float32, torch.bfloat16)
     _check_cuda(q, "q", fdt)
@@ -214,12 +223,25 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if workspace is not None:
         _check_cuda(workspace, "workspace", (torch.uint8,), dev)
+    fused = (k_new, v_new, slot_mapping)
+    if any(t is not None for t in fused):
+        if any(t is None for t in fused):
+            raise ValueError("k_new, v_new and slot_mapping go together")
+        _check_cuda(k_new, "k_new", (q.dtype,), dev)
+        _check_cuda(v_new, "v_new", (q.dtype,), dev)
+        _check_cuda(slot_mapping, "slot_mapping", (torch.int64,), dev)
+        if tuple(k_new.shape) != (S, Hkv, hd) or tuple(v_new.shape) != (S, Hkv, hd) or \
+                tuple(slot_mapping.shape) != (S,):
+            raise ValueError("k_new, v_new must be [S, Hkv, hd] and slot_mapping [S]")
     args = _DecodeArgs(S, block_tables.shape[1], nb, _dtype_code(q.dtype), partition_size,
                        max_context_len,
                        workspace.data_ptr() if workspace is not None else None,
                        workspace.numel() if workspace is not None else 0,
                        status.ptr() if status is not None else None,
-                       _stream_ptr(stream, dev), phase)
+                       _stream_ptr(stream, dev), phase,
+                       k_new.data_ptr() if k_new is not None else None,
+                       v_new.data_ptr() if v_new is not None else None,
+                       slot_mapping.data_ptr() if slot_mapping is not None else None)
     rc = _lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                         block_tables.data_ptr(), context_lens.data_ptr(), Hq, Hkv, hd, bs,
                         float(scale), ctypes.byref(args))

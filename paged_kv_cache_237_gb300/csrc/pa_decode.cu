@@ -140,7 +140,7 @@ __device__ void merge_and_store(const uint8_t *smem, int warp_bytes, const Decod
 
 // Describes the item a CTA is working on.
 struct Item {
-    int seq, part, kvh, qh0, rows;
+    int seq, part, kvh, ht, qh0, rows, n;
     int tok_begin, tok_end, nchunks;
     bool single;
 };
@@ -155,12 +155,14 @@ __device__ __forceinline__ bool next_item(Item &it, SeqCursor &cur, long long it
     it.seq = cur.seq;
     it.part = static_cast<int>(gp - cur.base);
     it.kvh = r / p.head_tiles;
+    it.ht = ht;
     it.qh0 = it.kvh * p.group + ht * tile_rows;
     it.rows = min(tile_rows, p.group - ht * tile_rows);
     const int raw = p.context_lens[it.seq];
     if (threadIdx.x == 0 && r == 0 && it.part == 0 && (raw < 0 || raw > p.ctx_cap))
         flag_status(p.status, PA_STATUS_BAD_CONTEXT_LEN);
     const int n = seq_len(p, it.seq);
+    it.n = n;
     it.tok_begin = it.part * p.partition_size;
     it.tok_end = min(n, it.tok_begin + p.partition_size);
     const int ntok = max(0, it.tok_end - it.tok_begin);
@@ -183,6 +185,33 @@ __device__ __forceinline__ int chunk_row(const DecodeParams &p, const Item &it, 
     }
     return static_cast<int>(((long long)phys * p.num_kv_heads + it.kvh) * p.block_size +
                             tok % p.block_size);
+}
+
+// The new token of a fused cache write, as one item sees it: the item's chunk
+// that holds position n - 1 (or -1), the row inside that chunk, and the row of
+// the [num_blocks * Hkv * block_size, head_dim] cache view to write.  Only the
+// last partition holds the new token; a slot that is not the slot of position
+// n - 1 is flagged once (KV head 0, head tile 0) and ignored.
+struct NewToken {
+    int chunk, row;
+    long long cache_row;
+};
+
+__device__ __forceinline__ NewToken new_token(const DecodeParams &p, const Item &it) {
+    NewToken t{-1, 0, -1};
+    if (!p.k_new || it.n <= 0 || it.tok_end != it.n) return t;
+    const int64_t slot = p.slot_mapping[it.seq];
+    if (slot < 0) return t;
+    const int pos = it.n - 1;
+    const int phys = p.block_tables[(long long)it.seq * p.max_blocks_per_seq + pos / p.block_size];
+    if (phys < 0 || phys >= p.num_blocks || slot != (int64_t)phys * p.block_size + pos % p.block_size) {
+        if (threadIdx.x == 0 && it.kvh == 0 && it.ht == 0) flag_status(p.status, PA_STATUS_BAD_SLOT);
+        return t;
+    }
+    t.chunk = (pos - it.tok_begin) / kChunk;
+    t.row = (pos - it.tok_begin) % kChunk;
+    t.cache_row = ((long long)phys * p.num_kv_heads + it.kvh) * p.block_size + pos % p.block_size;
+    return t;
 }
 
 // ------------------------------------------------------------ bf16 path ---
@@ -272,6 +301,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
         const int pro = my_n < NSTAGE ? my_n : NSTAGE;
         for (int k = 0; k < pro; ++k) issue(k);
+        const NewToken ntok = new_token(p, it);   // its loads overlap the copies in flight
 
         float o[NT][4];
 #pragma unroll
@@ -291,6 +321,28 @@ __global__ void __launch_bounds__(kWarps * 32)
             const uint32_t Ks = wbuf_s + s * STAGE_BYTES, Vs = Ks + PAGE_BYTES;
             const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
             const int valid = min(kChunk, it.tok_end - tok0);
+            if (warp + kWarps * k == ntok.chunk) {
+                // Fused cache write: put the new token's K/V row into the staged
+                // tile (whatever the copy read) and, once per (sequence, KV
+                // head), into the caches.
+                constexpr int V16 = HD / 8;   // 16-byte pieces per row
+                const long long src = ((long long)it.seq * p.num_kv_heads + it.kvh) * V16;
+                const uint4 *kn = static_cast<const uint4 *>(p.k_new) + src;
+                const uint4 *vn = static_cast<const uint4 *>(p.v_new) + src;
+                uint8_t *st = wbuf + s * STAGE_BYTES;
+                const int r = ntok.row;
+                for (int i = lane; i < 2 * V16; i += 32) {
+                    const bool isv = i >= V16;
+                    const int c = isv ? i - V16 : i;
+                    const uint4 val = isv ? vn[c] : kn[c];
+                    *reinterpret_cast<uint4 *>(st + (isv ? PAGE_BYTES : 0) + (c >> 3) * HALF_BYTES + r * 128 +
+                                               (((c & 7) ^ (r & 7)) << 4)) = val;
+                    if (it.ht == 0)
+                        static_cast<uint4 *>(isv ? p.v_cache_w : p.k_cache_w)[ntok.cache_row * V16 + c] = val;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             if (valid < kChunk) {
                 // Tokens past the context: zero their V rows so that p = 0
                 // multiplies exact zeros (the slots may hold anything, NaN too).
@@ -510,6 +562,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
         }
         const int pro = my_n < NSTAGE ? my_n : NSTAGE;
         for (int k = 0; k < pro; ++k) issue(k);
+        const NewToken ntok = new_token(p, it);
 
         float acc[HT][VEC], m[HT], l[HT];
 #pragma unroll
@@ -534,6 +587,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
             const float *Vs = Ks + kChunk * HD;
             const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
             const int valid = min(kChunk, it.tok_end - tok0);
+            if (warp + kWarps * k == ntok.chunk) {
+                // Fused cache write (see the bf16 kernel); plain row layout here.
+                constexpr int V4 = HD / 4;
+                const long long src = ((long long)it.seq * p.num_kv_heads + it.kvh) * V4;
+                const float4 *kn = static_cast<const float4 *>(p.k_new) + src;
+                const float4 *vn = static_cast<const float4 *>(p.v_new) + src;
+                float4 *st = reinterpret_cast<float4 *>(wbuf + s * STAGE_BYTES);
+                for (int i = lane; i < 2 * V4; i += 32) {
+                    const bool isv = i >= V4;
+                    const int c = isv ? i - V4 : i;
+                    const float4 val = isv ? vn[c] : kn[c];
+                    st[(isv ? kChunk * V4 : 0) + ntok.row * V4 + c] = val;
+                    if (it.ht == 0)
+                        static_cast<float4 *>(isv ? p.v_cache_w : p.k_cache_w)[ntok.cache_row * V4 + c] = val;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             for (int tt = 0; tt < valid; ++tt) {
                 float kv[VEC], vv[VEC];
 #pragma unroll
@@ -817,6 +888,12 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
         return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: partition_size must be a multiple of 16 in [16, 4096]");
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: out, q and caches must be 16-byte aligned");
+    const bool fused = a->k_new || a->v_new || a->slot_mapping;
+    if (fused && (!a->k_new || !a->v_new || !a->slot_mapping))
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: k_new, v_new and slot_mapping go together");
+    if (fused && (!aligned16(a->k_new) || !aligned16(a->v_new) ||
+                  (reinterpret_cast<uintptr_t>(a->slot_mapping) & 7u)))
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: k_new/v_new must be 16-byte and slot_mapping 8-byte aligned");
     const long long total_rows = static_cast<long long>(a->num_blocks) * num_kv_heads * block_size;
     if (total_rows >= INT_MAX) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: cache has 2^31 or more rows");
 
@@ -839,6 +916,11 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.status = a->dev_status;
+    p.k_new = a->k_new;
+    p.v_new = a->v_new;
+    p.slot_mapping = a->slot_mapping;
+    p.k_cache_w = const_cast<void *>(k_cache);
+    p.v_cache_w = const_cast<void *>(v_cache);
     p.num_seqs = a->num_seqs;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;

@@ -31,6 +31,11 @@ struct DecodeParams {
     float *part_ml;        // [S][max_parts][Hq][2]  (running max in log2 units, sum)
     float *part_acc;       // [S][max_parts][Hq][HD] (unnormalised)
     int32_t *status;
+    const void *k_new;     // fused cache write: [S][Hkv][HD] or nullptr
+    const void *v_new;
+    const int64_t *slot_mapping;
+    void *k_cache_w;       // writable views of the caches (fused write only)
+    void *v_cache_w;
     int num_seqs, num_q_heads, num_kv_heads, group, head_tiles, tile_rows;
     int block_size, num_blocks, max_blocks_per_seq;
     int partition_size, max_parts, ctx_cap;

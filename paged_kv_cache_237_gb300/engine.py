@@ -34,11 +34,22 @@ class DecodeStep:
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=q.device) if ws else None
         self.status = binding.DeviceStatus(q.device)
 
-    def decode(self, stream=None, phase: int = binding.PA_PHASE_ALL) -> torch.Tensor:
+    def decode(self, stream=None, phase: int = binding.PA_PHASE_ALL, k_new=None, v_new=None,
+               slot_mapping=None) -> torch.Tensor:
         return binding.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
                                  self.context_lens, self.scale, max_context_len=self.max_context_len,
                                  partition_size=self.partition_size, workspace=self.workspace,
-                                 status=self.status, stream=stream, phase=phase)
+                                 status=self.status, stream=stream, phase=phase, k_new=k_new,
+                                 v_new=v_new, slot_mapping=slot_mapping)
+
+    def run_fused(self, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                  cow_pairs: torch.Tensor | None = None, stream=None,
+                  phase: int = binding.PA_PHASE_ALL) -> torch.Tensor:
+        """Copy-on-write copies, then one decode launch that also writes each
+        sequence's new token (one token per sequence, slot of its last position)."""
+        if cow_pairs is not None and cow_pairs.numel() and phase != binding.PA_PHASE_REDUCE:
+            binding.pa_copy_blocks(self.k_cache, self.v_cache, cow_pairs, status=self.status, stream=stream)
+        return self.decode(stream, phase, k_new, v_new, slot_mapping)
 
     def write_tokens(self, k_new, v_new, slot_mapping, cow_pairs=None, stream=None) -> None:
         """The step's cache updates: copy-on-write copies, then the new rows."""

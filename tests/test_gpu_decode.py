@@ -136,3 +136,60 @@ def test_large_batch_many_items(pa):
     out = run(pa, q, kc, vc, tables, lens_t, 1 / math.sqrt(128), partition_size=256)
     ref = oracle_decode(q, kc, vc, tables, lens_t, 1 / math.sqrt(128))
     assert_decode_close(out, ref, torch.bfloat16, what="96 seqs")
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("hd,bs,Hq,Hkv", [(128, 16, 8, 1), (64, 32, 40, 2), (128, 32, 32, 8)])
+def test_fused_cache_write_matches_write_then_decode(pa, dtype, hd, bs, Hq, Hkv):
+    """One launch that writes each sequence's new token and attends with it gives
+    bit-identical outputs and caches to pa_reshape_and_cache then pa_decode.
+    Sequence 2 is padding (slot -1): neither path writes it."""
+    lens = [1, 16, 17, 40, 513, 1025, 2000]
+    q, kc, vc, tables, lens_t = make_case(lens, Hq, Hkv, hd, bs, dtype, seed=31 + hd + Hq)
+    S = len(lens)
+    g = torch.Generator().manual_seed(5)
+    k_new = torch.randn(S, Hkv, hd, generator=g).to(dtype).cuda()
+    v_new = torch.randn(S, Hkv, hd, generator=g).to(dtype).cuda()
+    tab = tables.cpu()
+    slots = torch.tensor([int(tab[i, (n - 1) // bs]) * bs + (n - 1) % bs for i, n in enumerate(lens)],
+                         dtype=torch.int64)
+    slots[2] = -1
+    slots = slots.cuda()
+    kc_a, vc_a = kc.clone(), vc.clone()
+    pa.pa_reshape_and_cache(k_new, v_new, kc_a, vc_a, slots)
+    out_a = run(pa, q, kc_a, vc_a, tables, lens_t, 0.1, partition_size=256)
+    status = pa.DeviceStatus()
+    out_b = torch.empty_like(q)
+    pa.pa_decode(out_b, q, kc, vc, tables, lens_t, 0.1, max_context_len=max(lens), partition_size=256,
+                 status=status, k_new=k_new, v_new=v_new, slot_mapping=slots)
+    torch.cuda.synchronize()
+    assert status.read() == 0
+    assert torch.equal(_bits(out_a), _bits(out_b))
+    assert torch.equal(_bits(kc_a), _bits(kc)) and torch.equal(_bits(vc_a), _bits(vc))
+    ref = oracle_decode(q, kc_a, vc_a, tables, lens_t, 0.1)
+    assert_decode_close(out_b, ref, dtype, what="fused")
+
+
+def test_fused_cache_write_rejects_a_slot_that_is_not_the_last_position(pa):
+    lens = [40, 40]
+    q, kc, vc, tables, lens_t = make_case(lens, 8, 2, 128, 16, torch.bfloat16, seed=3, nan_tails=False)
+    k_new = torch.ones(2, 2, 128, dtype=torch.bfloat16, device="cuda")
+    tab = tables.cpu()
+    good = int(tab[0, 39 // 16]) * 16 + 39 % 16
+    slots = torch.tensor([good, int(tab[1, 0]) * 16 + 3], dtype=torch.int64, device="cuda")  # seq 1: wrong slot
+    before = kc.clone()
+    status = pa.DeviceStatus()
+    out = torch.empty_like(q)
+    pa.pa_decode(out, q, kc, vc, tables, lens_t, 0.1, max_context_len=40, status=status,
+                 k_new=k_new, v_new=k_new, slot_mapping=slots)
+    torch.cuda.synchronize()
+    assert status.read() & pa.STATUS_BAD_SLOT
+    blk1 = tables[1].long()
+    assert torch.equal(_bits(kc[blk1]), _bits(before[blk1]))        # nothing written for sequence 1
+    assert kc[good // 16, :, good % 16].eq(1).all()                 # sequence 0 written
+    plain = run(pa, q, kc, vc, tables, lens_t, 0.1)
+    assert torch.equal(_bits(out[1]), _bits(plain[1]))

@@ -88,9 +88,14 @@ def test_long_context_full_size_sampled(pa):
     w = d["workload"]
     step = engine.DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                              d["scale"], d["max_context_len"], w.partition_size)
-    out = step.run(d["k_new"], d["v_new"], d["slot_mapping"])
+    out_sep = step.run(d["k_new"], d["v_new"], d["slot_mapping"]).clone()
     torch.cuda.synchronize()
     assert step.status.read() == 0
+    # the benchmark's step: one decode launch that also writes the new tokens
+    out = step.run_fused(d["k_new"], d["v_new"], d["slot_mapping"])
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    assert torch.equal(bits(out), bits(out_sep))
     lens = d["lens"]
     longs = [int(i) for i in np.flatnonzero(lens == 131072)[:2]]
     rng = np.random.default_rng(0)
