@@ -248,13 +248,22 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="write the new tokens with a separate pa_reshape_and_cache launch instead of inside "
                          "the decode launch")
-    ap.add_argument("--study", choices=["placement"], default=None,
+    ap.add_argument("--study", choices=["placement", "prefix_cache", "swap"], default=None,
                     help="instead of the benchmark line, print one study line: 'placement' times the partition "
-                         "pass with shuffled vs identity block placement at block sizes 32 and 16")
+                         "pass with shuffled vs identity block placement at block sizes 32 and 16; "
+                         "'prefix_cache' admits a multi-tenant batch through the chained-key prefix cache and "
+                         "times its decode step; 'swap' times block copies between the device cache and pinned "
+                         "host memory")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.study == "placement":
         run_placement_study(args)
+        return
+    if args.study == "prefix_cache":
+        run_prefix_cache_study(args)
+        return
+    if args.study == "swap":
+        run_swap_study(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -515,6 +524,122 @@ def run_placement_study(args):
            "gather_overhead_bs16": round(rows["bs16_shuffled"]["ms"] / rows["bs16_identity"]["ms"] - 1, 4),
            "bs16_vs_bs32_shuffled": round(rows["bs16_shuffled"]["ms"] / rows["bs32_shuffled"]["ms"] - 1, 4)}
     print(json.dumps(out), flush=True)
+
+
+def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_len: int = 2048):
+    """A multi-tenant batch admitted through the chained-key prefix cache: each
+    tenant has its own 2048-token system prompt (salted by tenant), each
+    request adds a private question of 16..512 tokens.  Reports host admission
+    cost, blocks held with and without sharing, and the decode step over the
+    shared blocks (GQA 64/8, head_dim 128, bs 16, bf16)."""
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    from paged_kv_cache_237_gb300.workloads import randn
+    torch.cuda.set_device(0)
+    rng = np.random.default_rng(7)
+    bs, Hq, Hkv, hd = 16, 64, 8, 128
+    systems = [rng.integers(0, 128000, size=prompt_len).tolist() for _ in range(tenants)]
+    reqs = []
+    for t in range(tenants):
+        for _ in range(per_tenant):
+            reqs.append((t, systems[t] + rng.integers(0, 128000, size=int(rng.integers(16, 513))).tolist()))
+    order = rng.permutation(len(reqs))
+    unshared = sum(-(-(len(r[1]) + 1) // bs) for r in reqs)
+    bm = binding.BlockManager(unshared + 64, bs)
+    t0 = time.perf_counter()
+    cached_tokens = 0
+    for sid in order:
+        t, toks = reqs[sid]
+        cached_tokens += bm.add_seq_cached(int(sid), toks, salt=1000 + t)
+    admit_s = time.perf_counter() - t0
+    seqs = list(range(len(reqs)))
+    slots, pairs = bm.append_slots(seqs)
+    held = bm.num_blocks - bm.num_free()
+    max_blocks = max(len(bm.block_table(s)) for s in seqs)
+    tables, lens = bm.build_tables(seqs, max_blocks)
+    dev = torch.device("cuda", 0)
+    nb = bm.num_blocks
+    q = randn((len(seqs), Hq, hd), torch.bfloat16, 71, dev)
+    kc = randn((nb, Hkv, bs, hd), torch.bfloat16, 72, dev)
+    vc = randn((nb, Hkv, bs, hd), torch.bfloat16, 73, dev)
+    kn = randn((len(seqs), Hkv, hd), torch.bfloat16, 74, dev)
+    vn = randn((len(seqs), Hkv, hd), torch.bfloat16, 75, dev)
+    step = DecodeStep(q, kc, vc, tables.to(dev), lens.to(dev), 1 / math.sqrt(hd), int(lens.max()))
+    sl = slots.to(dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run_fused(kn, vn, sl, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        step.run_fused(kn, vn, sl, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    logical = decode_bytes(lens.tolist(), Hq, Hkv, hd, bs, 2, 2, 2)
+    unique_kv = held * Hkv * bs * hd * 2 * 2
+    print(json.dumps({
+        "study": "prefix_cache", "tenants": tenants, "requests": len(reqs), "system_prompt_tokens": prompt_len,
+        "copy_on_write_pairs": int(pairs.shape[0]),
+        "host_admission_us_per_request": round(admit_s / len(reqs) * 1e6, 2),
+        "cached_tokens_at_admission": int(cached_tokens),
+        "blocks_held": int(held), "blocks_without_sharing": int(unshared),
+        "memory_saved": round(1 - held / unshared, 4),
+        "decode_step_ms": round(ms, 4), "logical_kv_GBps": round(logical / (ms * 1e-3) / 1e9, 1),
+        "unique_kv_bytes": int(unique_kv), "unique_kv_GBps": round(unique_kv / (ms * 1e-3) / 1e9, 1)}),
+        flush=True)
+
+
+def run_swap_study(args, num_blocks: int = 4096):
+    """Swap-out (device -> pinned host) and swap-in (host -> device) of
+    `num_blocks` scattered blocks of the long-context geometry (8 KV heads,
+    block_size 32, head_dim 128, bf16: 128 KB of K+V per block)."""
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.workloads import randn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    Hkv, bs, hd = 8, 32, 128
+    pool = 3 * num_blocks
+    dk = randn((pool, Hkv, bs, hd), torch.bfloat16, 81, dev)
+    dv = randn((pool, Hkv, bs, hd), torch.bfloat16, 82, dev)
+    hk = torch.empty((num_blocks, Hkv, bs, hd), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((num_blocks, Hkv, bs, hd), dtype=torch.bfloat16).pin_memory()
+    rng = np.random.default_rng(9)
+    dev_ids = rng.choice(pool, size=num_blocks, replace=False)
+    out_pairs = torch.from_numpy(np.stack([dev_ids, rng.permutation(num_blocks)], 1).astype(np.int64)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(num_blocks), rng.choice(pool, size=num_blocks, replace=False)],
+                                         1).astype(np.int64)).to(dev)
+    status = binding.DeviceStatus(dev)
+    stream = torch.cuda.current_stream()
+    nbytes = num_blocks * Hkv * bs * hd * 2 * 2
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms_out = timed(lambda: binding.pa_swap_blocks(dk, dv, hk, hv, out_pairs, status=status, stream=stream))
+    ms_in = timed(lambda: binding.pa_swap_blocks(hk, hv, dk, dv, in_pairs, status=status, stream=stream))
+    if status.read():
+        raise RuntimeError("device status flagged an input error")
+    print(json.dumps({"study": "swap", "blocks": num_blocks, "bytes_each_way": nbytes,
+                      "swap_out_ms": round(ms_out, 4), "swap_out_GBps": round(nbytes / (ms_out * 1e-3) / 1e9, 1),
+                      "swap_in_ms": round(ms_in, 4), "swap_in_GBps": round(nbytes / (ms_in * 1e-3) / 1e9, 1)}),
+          flush=True)
 
 
 def run_reference(args):

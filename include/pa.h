@@ -188,6 +188,22 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, i
                    int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
                    int32_t *dev_status, void *stream);
 
+/* ---- block swap between two pools (device cache <-> host memory) --------
+ * [P2] "Points cles" / "Termes employes sur cette page" (page eviction): when
+ * GPU memory runs out, cold pages are written to CPU RAM and read back when
+ * needed.  For each pair p, block dst_p of (dst_k, dst_v) becomes a bit-exact
+ * copy of block src_p of (src_k, src_v): every KV head and slot.  The two
+ * pools share the block geometry (num_kv_heads, block_size, head_dim, dtype)
+ * and must be different allocations; each may be device memory or pinned host
+ * memory the device can address (cudaHostAlloc / cudaHostRegister; checked
+ * with cudaPointerGetAttributes, anything else is PA_ERR_INVALID_ARG).
+ * src_dst_pairs must be device-accessible as well.  A pair out of range, or a
+ * dst named twice, is skipped and sets PA_STATUS_BAD_PAIR. */
+int pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                   const int64_t *src_dst_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
+                   int num_kv_heads, int head_dim, int block_size, int dtype, int32_t *dev_status,
+                   void *stream);
+
 /* ---- host block manager -----------------------------------------------
  * [P3] "Komponenty": a block manager hands out and takes back physical
  * blocks from a free pool and keeps per-block reference counts for shared
@@ -231,8 +247,48 @@ int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap);
 
 /* Tokens the sequence holds, or a negative error code. */
 int pa_bm_num_tokens(const pa_bm *bm, int seq_id);
-int pa_bm_num_free(const pa_bm *bm);
+int pa_bm_num_free(const pa_bm *bm);   /* free plus cached (both can be handed out) */
 int pa_bm_refcount(const pa_bm *bm, int block); /* negative if out of range */
+
+/* ---- automatic prefix caching (chained block hash, tenant salt) --------
+ * [P4] "Deux couches, pas deux rivaux": every full block is keyed by a hash of
+ * its parent block's key, its own tokens and optional extra data, so equal
+ * token prefixes give equal key chains and find blocks already computed;
+ * [P4] "Au-dela": a per-tenant salt mixed into the key keeps tenants apart.
+ *
+ * key_0 = H(0, salt, tokens[0..bs)), key_i = H(key_{i-1}, salt, tokens of block i),
+ * H = 64-bit FNV-1a over the little-endian bytes of (parent key u64, salt u64,
+ * each token as int32).  A key hit also compares the stored tokens, so hash
+ * collisions cannot alias blocks.  Only full blocks are keyed.  A keyed block
+ * whose refcount drops to zero stays cached (its K/V intact) and can be reused
+ * by a later request until the pool runs short: allocation takes a free block
+ * first, then evicts the least recently released cached block. */
+
+/* New sequence of n tokens: leading full blocks whose keys are cached are
+ * shared (refcount + 1); the rest are fresh, and the fresh full blocks are
+ * keyed.  *num_cached_tokens = tokens whose K/V are already present (the
+ * caller must compute and write the others before any other request can use
+ * the newly keyed blocks).  PA_ERR_NO_BLOCKS leaves the state unchanged. */
+int pa_bm_add_seq_cached(pa_bm *bm, int seq_id, const int32_t *tokens, int n, uint64_t salt,
+                         int *num_cached_tokens);
+
+/* Key the sequence's full blocks that are not keyed yet (for example after
+ * decoding filled a block); tokens[0..n) are the sequence's tokens, n equal
+ * to its length.  A block whose key already names another cached block stays
+ * private.  Returns the number of blocks newly keyed, or an error code. */
+int pa_bm_register_blocks(pa_bm *bm, int seq_id, const int32_t *tokens, int n, uint64_t salt);
+
+/* Blocks held only by the cache (refcount 0, reusable on a hit). */
+int pa_bm_num_cached(const pa_bm *bm);
+
+/* Move a sequence from one manager to another (a device pool and a host pool
+ * of the same block size): every block gets a fresh block in `to`, the pairs
+ * (from block, to block) are written to pairs[2 * k], pairs[2 * k + 1] for the
+ * caller's pa_swap_blocks, and the blocks in `from` are released.  All of the
+ * sequence's blocks must be unshared (refcount 1): PA_ERR_REFCOUNT otherwise.
+ * PA_ERR_NO_BLOCKS if `to` is short; *num_pairs = blocks moved; cap is the
+ * room of pairs in pairs.  On failure nothing changes. */
+int pa_bm_move_seq(pa_bm *from, pa_bm *to, int seq_id, int64_t *pairs, int cap, int *num_pairs);
 
 /* Batched decode-step helper: append one slot to each of n sequences in order.
  * slots[k] receives the slot of seq_ids[k]; copy pairs are appended to
@@ -246,6 +302,15 @@ int pa_bm_append_slots(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots,
  * tables [n][max_blocks_per_seq] (unused entries = -1), context_lens [n]. */
 int pa_bm_build_tables(const pa_bm *bm, const int32_t *seq_ids, int n, int32_t *tables,
                        int max_blocks_per_seq, int32_t *context_lens);
+
+/* ---- self-test of the bounded wait ----------------------------------------
+ * Every wait of the decode kernels for staged data gives up after about two
+ * seconds, sets PA_STATUS_WAIT_TIMEOUT and lets the kernel finish, so a copy
+ * that never lands cannot hang the GPU.  This call runs that same wait in a
+ * one-thread kernel on a barrier that nothing completes, with a limit of
+ * limit_us microseconds (1..1000000), and ORs PA_STATUS_WAIT_TIMEOUT into
+ * *dev_status when it gives up (it always does).  For tests of that path. */
+int pa_selftest_wait_timeout(int32_t *dev_status, int limit_us, void *stream);
 
 /* ---- misc --------------------------------------------------------------- */
 const char *pa_last_error_string(void); /* thread-local, never NULL */

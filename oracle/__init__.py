@@ -65,6 +65,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     lib.oracle_copy_blocks.restype = i32
     lib.oracle_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
+    lib.oracle_swap_blocks.restype = i32
+    lib.oracle_swap_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32]
     return lib
 
 
@@ -175,3 +177,18 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
     rc = lib.oracle_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pr.data_ptr(),
                                 pr.shape[0], Hkv, hd, bs, nb, k_cache.element_size())
     _check(rc, "copy_blocks")
+
+
+def swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                src_dst_pairs: torch.Tensor, lib: ctypes.CDLL | None = None) -> None:
+    """In-place block copy between two CPU pools of the same geometry."""
+    lib = lib or load()
+    for t in (src_k, src_v, dst_k, dst_v):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("pools must be contiguous CPU tensors")
+    pr = _cpu(src_dst_pairs, (torch.int64,), "src_dst_pairs")
+    nbs, Hkv, bs, hd = src_k.shape
+    nbd = dst_k.shape[0]
+    rc = lib.oracle_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
+                                pr.data_ptr(), pr.shape[0], nbs, nbd, Hkv, hd, bs, src_k.element_size())
+    _check(rc, "swap_blocks")

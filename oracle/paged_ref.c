@@ -313,3 +313,29 @@ int oracle_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pair
     }
     return ORACLE_OK;
 }
+
+/* Block copy between two pools of the same geometry (swap to or from host
+ * memory): block dst of (dst_k, dst_v) becomes a copy of block src of
+ * (src_k, src_v), pairs applied in list order.  ("PagedAttention" concept
+ * sheet, analyticslegends.ai, "Points cles": cold pages go to CPU RAM and are
+ * read back on demand.) */
+int oracle_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                       const int64_t *src_dst_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
+                       int num_kv_heads, int head_dim, int block_size, int elem_bytes)
+{
+    if (!src_k || !src_v || !dst_k || !dst_v || (num_pairs > 0 && !src_dst_pairs) || num_pairs < 0 ||
+        num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || (elem_bytes != 2 && elem_bytes != 4))
+        return ORACLE_ERR_ARG;
+    for (int p = 0; p < num_pairs; ++p) {
+        int64_t s = src_dst_pairs[2 * p], d = src_dst_pairs[2 * p + 1];
+        if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks)
+            return ORACLE_ERR_INDEX;
+    }
+    size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * elem_bytes;
+    for (int p = 0; p < num_pairs; ++p) {
+        int64_t s = src_dst_pairs[2 * p], d = src_dst_pairs[2 * p + 1];
+        memcpy((char *)dst_k + d * block_bytes, (const char *)src_k + s * block_bytes, block_bytes);
+        memcpy((char *)dst_v + d * block_bytes, (const char *)src_v + s * block_bytes, block_bytes);
+    }
+    return ORACLE_OK;
+}

@@ -80,6 +80,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     lib.pa_copy_blocks.restype = i32
     lib.pa_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_swap_blocks.restype = i32
+    lib.pa_swap_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_bm_move_seq.restype = i32
+    lib.pa_bm_move_seq.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32)]
+    lib.pa_selftest_wait_timeout.restype = i32
+    lib.pa_selftest_wait_timeout.argtypes = [vp, i32, vp]
     lib.pa_bm_create.restype = vp
     lib.pa_bm_create.argtypes = [i32, i32]
     lib.pa_bm_destroy.restype = None
@@ -103,6 +109,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pa_bm_refcount.argtypes = [vp, i32]
     lib.pa_bm_append_slots.restype = i32
     lib.pa_bm_append_slots.argtypes = [vp, vp, i32, vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.pa_bm_add_seq_cached.restype = i32
+    lib.pa_bm_add_seq_cached.argtypes = [vp, i32, vp, i32, ctypes.c_uint64, ctypes.POINTER(i32)]
+    lib.pa_bm_register_blocks.restype = i32
+    lib.pa_bm_register_blocks.argtypes = [vp, i32, vp, i32, ctypes.c_uint64]
+    lib.pa_bm_num_cached.restype = i32
+    lib.pa_bm_num_cached.argtypes = [vp]
     lib.pa_bm_build_tables.restype = i32
     lib.pa_bm_build_tables.argtypes = [vp, vp, i32, vp, i32, vp]
     lib.pa_last_error_string.restype = ctypes.c_char_p
@@ -287,6 +299,35 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: 
     _raise(rc)
 
 
+def pa_swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                   src_dst_pairs: torch.Tensor, *, status: DeviceStatus | None = None, stream=None) -> None:
+    """Copy whole blocks between two pools of the same geometry, each on the
+    GPU or in pinned host memory (swap out / swap in).  src_dst_pairs [P, 2]
+    int64, on the GPU or pinned."""
+    pools = (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v))
+    for name, t in pools:
+        if not isinstance(t, torch.Tensor) or t.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError(f"{name} must be an fp32 or bf16 tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous [num_blocks, Hkv, bs, hd] tensor")
+        if t.device.type == "cpu" and not t.is_pinned():
+            raise ValueError(f"{name} is pageable host memory; pin it (pin_memory()) so the GPU can address it")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_v.shape != src_k.shape or dst_v.shape != dst_k.shape \
+            or len({t.dtype for _, t in pools}) != 1:
+        raise ValueError("pools must share block geometry and dtype")
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be int64 [P, 2]")
+    if src_dst_pairs.device.type == "cpu" and not src_dst_pairs.is_pinned():
+        raise ValueError("src_dst_pairs must be on the GPU or pinned")
+    dev = next((t.device for _, t in pools if t.device.type == "cuda"), torch.device("cuda"))
+    nbs, Hkv, bs, hd = src_k.shape
+    rc = _lib.pa_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
+                             src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], nbs, dst_k.shape[0], Hkv, hd, bs,
+                             _dtype_code(src_k.dtype), status.ptr() if status is not None else None,
+                             _stream_ptr(stream, dev))
+    _raise(rc)
+
+
 class BlockManager:
     """Host block manager (``pa_bm_*``): free pool, refcounts, copy-on-write."""
 
@@ -332,6 +373,39 @@ class BlockManager:
                                      ctypes.byref(npairs), ctypes.byref(ndone))
         _raise(rc)
         return slots, pairs[:npairs.value].clone()
+
+    def add_seq_cached(self, seq_id: int, tokens, salt: int = 0) -> int:
+        """New sequence over token ids, sharing cached prefix blocks (chained
+        block keys, tenant salt).  Returns the number of leading tokens whose
+        K/V are already in the cache."""
+        t = torch.as_tensor(list(tokens) if not isinstance(tokens, torch.Tensor) else tokens,
+                            dtype=torch.int32).contiguous()
+        cached = ctypes.c_int()
+        _raise(_lib.pa_bm_add_seq_cached(self._h, seq_id, t.data_ptr() if t.numel() else None, t.numel(),
+                                         ctypes.c_uint64(salt & (2**64 - 1)), ctypes.byref(cached)))
+        return cached.value
+
+    def register_blocks(self, seq_id: int, tokens, salt: int = 0) -> int:
+        """Key the sequence's full blocks not keyed yet; returns how many."""
+        t = torch.as_tensor(list(tokens) if not isinstance(tokens, torch.Tensor) else tokens,
+                            dtype=torch.int32).contiguous()
+        n = _lib.pa_bm_register_blocks(self._h, seq_id, t.data_ptr() if t.numel() else None, t.numel(),
+                                       ctypes.c_uint64(salt & (2**64 - 1)))
+        if n < 0:
+            _raise(n)
+        return n
+
+    def num_cached(self) -> int:
+        return _lib.pa_bm_num_cached(self._h)
+
+    def move_seq(self, to: "BlockManager", seq_id: int) -> torch.Tensor:
+        """Move a sequence into another manager's pool; returns the int64
+        [P, 2] (block here, block there) pairs for pa_swap_blocks."""
+        cap = max(1, len(self.block_table(seq_id)))
+        pairs = torch.empty(cap, 2, dtype=torch.int64)
+        n = ctypes.c_int()
+        _raise(_lib.pa_bm_move_seq(self._h, to._h, seq_id, pairs.data_ptr(), cap, ctypes.byref(n)))
+        return pairs[:n.value].clone()
 
     def free_seq(self, seq_id: int) -> None:
         _raise(_lib.pa_bm_free_seq(self._h, seq_id))

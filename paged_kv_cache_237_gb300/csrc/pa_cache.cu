@@ -90,11 +90,72 @@ __global__ void __launch_bounds__(256)
     for (; i < block_vecs; i += blockDim.x) to[i] = from[i];
 }
 
+// grid (num_pairs, 2): copy whole blocks between two pools (blockIdx.y: K or
+// V).  Either side may be pinned host memory; the same 16-byte vector loop as
+// copy_blocks_kernel.  A dst named by another pair is skipped and flagged.
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(const uint4 *__restrict__ src_k, const uint4 *__restrict__ src_v,
+                       uint4 *__restrict__ dst_k, uint4 *__restrict__ dst_v, const int64_t *__restrict__ pairs,
+                       int num_pairs, long long block_vecs, int src_num_blocks, int dst_num_blocks,
+                       int32_t *status) {
+    const int pidx = blockIdx.x;
+    const int64_t src = pairs[2 * pidx], dst = pairs[2 * pidx + 1];
+    __shared__ int conflict;
+    if (threadIdx.x == 0) conflict = 0;
+    __syncthreads();
+    if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag_status(status, PA_STATUS_BAD_PAIR);
+        return;
+    }
+    for (int j = threadIdx.x; j < num_pairs; j += blockDim.x)
+        if (j != pidx && pairs[2 * j + 1] == dst) conflict = 1;
+    __syncthreads();
+    if (conflict) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag_status(status, PA_STATUS_BAD_PAIR);
+        return;
+    }
+    const uint4 *from = (blockIdx.y == 0 ? src_k : src_v) + src * block_vecs;
+    uint4 *to = (blockIdx.y == 0 ? dst_k : dst_v) + dst * block_vecs;
+    long long i = threadIdx.x;
+    for (; i + 3 * blockDim.x < block_vecs; i += 4 * blockDim.x) {
+        const uint4 a = from[i], b = from[i + blockDim.x], c = from[i + 2 * blockDim.x],
+                    d = from[i + 3 * blockDim.x];
+        to[i] = a;
+        to[i + blockDim.x] = b;
+        to[i + 2 * blockDim.x] = c;
+        to[i + 3 * blockDim.x] = d;
+    }
+    for (; i < block_vecs; i += blockDim.x) to[i] = from[i];
+}
+
+// One thread waits on a fresh barrier that no one arrives at; the bounded wait
+// must give up and report it.
+__global__ void wait_timeout_selftest_kernel(int32_t *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(b, 0, limit_ns)) flag_status(status, PA_STATUS_WAIT_TIMEOUT);
+}
+
 }  // namespace pa
 
 namespace {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : (dtype == PA_BF16 ? 2 : 0); }
+
+// True when the device can address `p`: device or managed memory, or pinned
+// host memory with a device mapping equal to the host pointer (unified
+// addressing).  Pageable host memory is refused rather than risked.
+bool device_addressable(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
 }  // namespace
 
 extern "C" int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
@@ -141,6 +202,49 @@ extern "C" int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_d
     pa::copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, num_pairs,
         block_bytes / 16, num_blocks, dev_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
+    return PA_OK;
+}
+
+extern "C" int pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                              const int64_t *src_dst_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
+                              int num_kv_heads, int head_dim, int block_size, int dtype, int32_t *dev_status,
+                              void *stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: bad dtype");
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || src_num_blocks <= 0 ||
+        dst_num_blocks <= 0)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: bad sizes");
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: null pointer");
+    if (src_k == dst_k || src_v == dst_v)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: source and destination pools must differ (use pa_copy_blocks)");
+    const long long block_bytes = static_cast<long long>(num_kv_heads) * block_size * head_dim * eb;
+    if (block_bytes % 16 != 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_swap_blocks: block bytes must be a multiple of 16");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) ||
+        (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u))
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: misaligned pointer");
+    if (!device_addressable(src_k) || !device_addressable(src_v) || !device_addressable(dst_k) ||
+        !device_addressable(dst_v) || !device_addressable(src_dst_pairs))
+        return pa_fail(PA_ERR_INVALID_ARG,
+                       "pa_swap_blocks: every pool and the pair list must be device memory or pinned host memory");
+    dim3 grid(num_pairs, 2);
+    pa::swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
+        static_cast<uint4 *>(dst_v), src_dst_pairs, num_pairs, block_bytes / 16, src_num_blocks, dst_num_blocks,
+        dev_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
+    return PA_OK;
+}
+
+extern "C" int pa_selftest_wait_timeout(int32_t *dev_status, int limit_us, void *stream) {
+    if (!dev_status || limit_us < 1 || limit_us > 1000000)
+        return pa_fail(PA_ERR_INVALID_ARG, "pa_selftest_wait_timeout: need a status word and 1 <= limit_us <= 1e6");
+    pa::wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+        dev_status, static_cast<uint64_t>(limit_us) * 1000ull);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
     return PA_OK;

@@ -83,14 +83,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete, giving up after about
-// two seconds so that a lost copy can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bounded waits give up after ~2 s
+
+// Wait for the phase with the given parity to complete, giving up after
+// limit_ns so that a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_timer_ns();
     for (uint32_t spin = 0;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0 && global_timer_ns() - start > 2000000000ull) return false;
+        if ((spin & 255u) == 0 && global_timer_ns() - start > limit_ns) return false;
     }
 }
 

@@ -84,3 +84,21 @@ def test_copy_blocks_rejects_racing_and_out_of_range_pairs(pa):
     assert got[2] == 2.0          # skipped: its dst is another pair's src
     assert got[3] == 2.0          # pair 1 copied the untouched block 2
     assert got[5] == 4.0          # valid pair applied
+
+
+def test_bounded_wait_gives_up_and_reports(pa):
+    """The decode kernels' bounded wait, on a barrier nothing completes, gives
+    up after its limit, flags PA_STATUS_WAIT_TIMEOUT and lets the kernel end;
+    the context stays usable."""
+    import ctypes
+    import time
+    status = pa.DeviceStatus()
+    t0 = time.perf_counter()
+    rc = pa._lib.pa_selftest_wait_timeout(ctypes.c_void_p(status.ptr()), 20000, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert status.read() & pa.STATUS_WAIT_TIMEOUT
+    assert 0.015 < dt < 5.0
+    x = torch.ones(1024, device="cuda")
+    assert float((x * 2).sum()) == 2048.0       # the GPU still runs work

@@ -112,3 +112,38 @@ def test_long_context_full_size_sampled(pa):
         assert torch.equal(bits(row.cpu()), bits(d["k_new"][s].cpu()))
     del d, step, out
     torch.cuda.empty_cache()
+
+
+def test_prefix_cached_batch_decodes_like_private_copies(pa):
+    """Requests admitted through the chained-key prefix cache (two tenants, one
+    system prompt each, salted) share their prompt blocks; one fused decode
+    step over the shared tables matches the oracle."""
+    binding, engine, workloads = pa
+    rng = np.random.default_rng(5)
+    bs, Hq, Hkv, hd = 16, 16, 2, 128
+    systems = [rng.integers(0, 1000, size=600).tolist() for _ in range(2)]
+    bm = binding.BlockManager(400, bs)
+    reqs = []
+    for sid in range(12):
+        t = sid % 2
+        toks = systems[t] + rng.integers(0, 1000, size=int(rng.integers(1, 60))).tolist()
+        hit = bm.add_seq_cached(sid, toks, salt=t)
+        assert hit == (0 if sid < 2 else 592)        # 37 full blocks of the 600-token prompt
+        reqs.append(toks)
+    seqs = list(range(12))
+    slots, pairs = bm.append_slots(seqs)
+    assert pairs.numel() == 0
+    tables, lens = bm.build_tables(seqs, max(len(bm.block_table(s)) for s in seqs))
+    g = torch.Generator().manual_seed(3)
+    kc = torch.randn(400, Hkv, bs, hd, generator=g).to(torch.bfloat16)
+    vc = torch.randn(400, Hkv, bs, hd, generator=g).to(torch.bfloat16)
+    q = torch.randn(12, Hq, hd, generator=g).to(torch.bfloat16)
+    kn = torch.randn(12, Hkv, hd, generator=g).to(torch.bfloat16)
+    vn = torch.randn(12, Hkv, hd, generator=g).to(torch.bfloat16)
+    step = engine.DecodeStep(q.cuda(), kc.cuda(), vc.cuda(), tables.cuda(), lens.cuda(), 0.09, int(lens.max()))
+    out = step.run_fused(kn.cuda(), vn.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    oracle.reshape_and_cache(kn, vn, kc, vc, slots)
+    ref = oracle_decode(q, kc, vc, tables, lens, 0.09)
+    assert_decode_close(out, ref, torch.bfloat16, what="prefix-cached batch")
