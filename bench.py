@@ -42,7 +42,7 @@ L2_BYTES = 129 * 2**20
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
 # batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
 # attended tokens.  Valid only while the kernel source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "500ab37f20fe44ad", "bytes": 918.15e6, "tokens": 219876,
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "b67df317039bd2b9", "bytes": 919.07e6, "tokens": 219876,
                    "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
 
 

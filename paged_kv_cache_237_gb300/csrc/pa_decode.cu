@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -759,25 +760,28 @@ EncodeTiledFn encode_tiled() {
 }
 
 int sm_count(int dev) {
-    static int cache[kMaxDevices] = {0};
+    static std::atomic<int> cache[kMaxDevices];
     if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
-// Per-kernel launch facts: dynamic smem set once, occupancy cached per device.
+// Per-kernel launch facts: dynamic smem set once, occupancy cached per device
+// (guarded, so concurrent first calls from several host threads are safe).
 struct KernelSlot {
     int smem = 0;
     int occupancy[kMaxDevices] = {0};
+    std::mutex mu;
 };
 
 template <typename K>
 int ensure_kernel(K kernel, KernelSlot &slot, int smem, int dev) {
     if (dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(slot.mu);
     if (slot.occupancy[dev] == 0) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return 0;
