@@ -312,48 +312,82 @@ def main():
              and bool(np.array_equal(last_slots, d["slot_mapping"].cpu().numpy())))
     new_tok = (d["k_new"], d["v_new"], d["slot_mapping"]) if fused else (None, None, None)
 
-    def one_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def cache_updates(st):
         if fused:
             if cow is not None and cow.numel():
-                binding.pa_copy_blocks(step.k_cache, step.v_cache, cow, status=step.status, stream=stream)
+                binding.pa_copy_blocks(step.k_cache, step.v_cache, cow, status=step.status, stream=st)
         else:
-            step.write_tokens(d["k_new"], d["v_new"], d["slot_mapping"], cow, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        step.decode(stream, binding.PA_PHASE_PARTITIONS, *new_tok)
-        if ev is not None:
-            ev[2].record(stream)
-        step.decode(stream, binding.PA_PHASE_REDUCE)
-        if ev is not None:
-            ev[3].record(stream)
+            step.write_tokens(d["k_new"], d["v_new"], d["slot_mapping"], cow, st)
+
+    def partition_pass(st):
+        step.decode(st, binding.PA_PHASE_PARTITIONS, *new_tok)
+
+    def merge(st):
+        step.decode(st, binding.PA_PHASE_REDUCE)
+
+    def one_step(st):
+        cache_updates(st)
+        partition_pass(st)
+        merge(st)
 
     for _ in range(args.warmup):
-        one_step()
+        one_step(stream)
         flush_l2(flush)
     torch.cuda.synchronize(device)
     if step.status.read():
         raise RuntimeError("device status flagged an input error")
 
+    # The timed step is a CUDA graph of the step's launches (how a decode loop
+    # runs in production): replays leave no host gaps between kernels, so the
+    # events measure the GPU alone.  Single-phase graphs time the phases.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn(None)
+        return g
+
+    has_updates = (not fused and d["slot_mapping"].numel() > 0) or (cow is not None and cow.numel() > 0)
+    g_step, g_part = capture(one_step), capture(partition_pass)
+    g_merge = capture(merge) if split else None
+    g_upd = capture(cache_updates) if has_updates else None
+
+    def timed_replays(g, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            flush_l2(flush)
+        torch.cuda.synchronize(device)
+        return [a.elapsed_time(b) for a, b in ev]
+
     K = args.steps
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for g in (g_step, g_part, g_merge, g_upd):
+        if g is not None:
+            timed_replays(g, 2)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(device)
     clocks = ClockSampler(local_rank)
     time.sleep(0.2)
-    for i in range(K):
-        one_step(events[i])
-        flush_l2(flush)
-    torch.cuda.synchronize(device)
+    step_ms = timed_replays(g_step, K)
     clk = clocks.stop()
     if dist is not None:
         dist.barrier()
-    step_ms = [e[0].elapsed_time(e[3]) for e in events]
-    part_ms = [e[1].elapsed_time(e[2]) for e in events]
-    red_ms = [e[2].elapsed_time(e[3]) for e in events]
-    write_ms = [e[0].elapsed_time(e[1]) for e in events]
+    part_ms = timed_replays(g_part, K)
+    red_ms = timed_replays(g_merge, K) if g_merge is not None else [0.0]
+    write_ms = timed_replays(g_upd, K) if g_upd is not None else [0.0]
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+    # the same step launched eagerly from Python, for comparison
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        a.record(stream)
+        one_step(stream)
+        b.record(stream)
+        flush_l2(flush)
+    torch.cuda.synchronize(device)
+    eager_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms, B_job = combine_ranks(statistics.mean(step_ms), B, dist, device)
     launches_per_step = (0 if fused or not d["slot_mapping"].numel() else 1) + 1 + (1 if split else 0) + \
         (1 if cow is not None and cow.numel() else 0)
@@ -454,6 +488,8 @@ def main():
         "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
         "step": "copy-on-write copies + decode launch that also writes the new tokens + split-K merge" if fused
                 else "copy-on-write copies + cache write + decode + split-K merge",
+        "timing": "CUDA graph of the step replayed; events around each replay",
+        "eager_ms_per_step": round(eager_ms, 4),
         "phases_ms": {"cache_updates": round(statistics.mean(write_ms), 4),
                       "partition_pass": round(part_avg, 4), "split_k_reduce": round(statistics.mean(red_ms), 4)},
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)" if w.dtype == torch.bfloat16
@@ -636,9 +672,24 @@ def run_swap_study(args, num_blocks: int = 4096):
     ms_in = timed(lambda: binding.pa_swap_blocks(hk, hv, dk, dv, in_pairs, status=status, stream=stream))
     if status.read():
         raise RuntimeError("device status flagged an input error")
+    # the copy engines on one contiguous range of the same size, for comparison
+    half = hk.numel()
+    dflat_k, dflat_v = dk.view(-1)[:half], dv.view(-1)[:half]
+    hflat_k, hflat_v = hk.view(-1), hv.view(-1)
+
+    def memcpy_out():
+        hflat_k.copy_(dflat_k, non_blocking=True)
+        hflat_v.copy_(dflat_v, non_blocking=True)
+
+    def memcpy_in():
+        dflat_k.copy_(hflat_k, non_blocking=True)
+        dflat_v.copy_(hflat_v, non_blocking=True)
+    mc_out, mc_in = timed(memcpy_out), timed(memcpy_in)
     print(json.dumps({"study": "swap", "blocks": num_blocks, "bytes_each_way": nbytes,
                       "swap_out_ms": round(ms_out, 4), "swap_out_GBps": round(nbytes / (ms_out * 1e-3) / 1e9, 1),
-                      "swap_in_ms": round(ms_in, 4), "swap_in_GBps": round(nbytes / (ms_in * 1e-3) / 1e9, 1)}),
+                      "swap_in_ms": round(ms_in, 4), "swap_in_GBps": round(nbytes / (ms_in * 1e-3) / 1e9, 1),
+                      "contiguous_memcpy_out_GBps": round(nbytes / (mc_out * 1e-3) / 1e9, 1),
+                      "contiguous_memcpy_in_GBps": round(nbytes / (mc_in * 1e-3) / 1e9, 1)}),
           flush=True)
 
 
