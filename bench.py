@@ -166,6 +166,25 @@ def combine_ranks(ms_local: float, bytes_local: int, dist=None, device="cpu"):
     return float(t.item()), int(b.item())
 
 
+def workload_config(w, d, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    lens = d["lens"]
+    elem = torch.tensor([], dtype=w.dtype).element_size()
+    working_set = d["k_cache"].numel() * elem * 2
+    return {
+        "workload": w.name,
+        "num_seqs": len(lens), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": w.partition_size,
+        "total_context_tokens": int(sum(int(n) for n in lens)),
+        "max_context_len": int(d["max_context_len"]),
+        "bytes_per_step": decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                       elem, elem, elem),
+        "l2": "inputs larger than L2 (no flush)" if working_set > 2 * L2_BYTES
+              else "512 MB L2 flush between steps",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 def flush_l2(buf):
     if buf is not None:
         buf.add_(1)
@@ -474,16 +493,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
-        "config": {
-            "workload": w.name,
-            "num_seqs": len(lens), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-            "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": w.partition_size,
-            "total_context_tokens": int(sum(int(n) for n in lens)),
-            "max_context_len": int(d["max_context_len"]),
-            "bytes_per_step": B,
-            "l2": "inputs larger than L2 (no flush)" if flush is None else "512 MB L2 flush between steps",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": workload_config(w, d, world),
         "hbm_fraction": round(B / (ms * 1e-3) / 1e9 / peak, 4),
         "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
         "step": "copy-on-write copies + decode launch that also writes the new tokens + split-K merge" if fused
@@ -730,8 +740,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "num_seqs": len(lens), "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size},
+        "config": workload_config(w, d, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
