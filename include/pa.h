@@ -16,7 +16,9 @@
  *    slot_mapping, src_dst_pairs, workspace and dev_status are DEVICE pointers
  *    owned by the caller.  The library never allocates device memory.
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
- *    stream.  Device calls only enqueue work and return before it runs.
+ *    stream.  Device calls only enqueue work and return before it runs.  They
+ *    launch on the calling thread's current CUDA device: every device pointer
+ *    (and the stream) must belong to it.
  *  - Every call returns PA_OK (0) or a negative PA_ERR_* code; nothing is
  *    thrown across the ABI.  pa_last_error_string() describes the last failure
  *    of the calling thread.

@@ -254,9 +254,10 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
                        k_new.data_ptr() if k_new is not None else None,
                        v_new.data_ptr() if v_new is not None else None,
                        slot_mapping.data_ptr() if slot_mapping is not None else None)
-    rc = _lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                        block_tables.data_ptr(), context_lens.data_ptr(), Hq, Hkv, hd, bs,
-                        float(scale), ctypes.byref(args))
+    with torch.cuda.device(dev):
+        rc = _lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                            block_tables.data_ptr(), context_lens.data_ptr(), Hq, Hkv, hd, bs,
+                            float(scale), ctypes.byref(args))
     _raise(rc)
     return out
 
@@ -274,11 +275,12 @@ def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor
     T = slot_mapping.shape[0]
     if tuple(k.shape) != (T, Hkv, hd) or tuple(v.shape) != (T, Hkv, hd) or v_cache.shape != k_cache.shape:
         raise ValueError("inconsistent shapes")
-    rc = _lib.pa_reshape_and_cache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                   slot_mapping.data_ptr(), T, Hkv, hd, bs, nb,
-                                   _dtype_code(k_cache.dtype),
-                                   status.ptr() if status is not None else None,
-                                   _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        rc = _lib.pa_reshape_and_cache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       slot_mapping.data_ptr(), T, Hkv, hd, bs, nb,
+                                       _dtype_code(k_cache.dtype),
+                                       status.ptr() if status is not None else None,
+                                       _stream_ptr(stream, dev))
     _raise(rc)
 
 
@@ -292,10 +294,11 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: 
     if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2 or v_cache.shape != k_cache.shape:
         raise ValueError("inconsistent shapes")
     nb, Hkv, bs, hd = k_cache.shape
-    rc = _lib.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), src_dst_pairs.data_ptr(),
-                             src_dst_pairs.shape[0], Hkv, hd, bs, nb, _dtype_code(k_cache.dtype),
-                             status.ptr() if status is not None else None,
-                             _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        rc = _lib.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), src_dst_pairs.data_ptr(),
+                                 src_dst_pairs.shape[0], Hkv, hd, bs, nb, _dtype_code(k_cache.dtype),
+                                 status.ptr() if status is not None else None,
+                                 _stream_ptr(stream, dev))
     _raise(rc)
 
 
@@ -319,12 +322,18 @@ def pa_swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor
         raise ValueError("src_dst_pairs must be int64 [P, 2]")
     if src_dst_pairs.device.type == "cpu" and not src_dst_pairs.is_pinned():
         raise ValueError("src_dst_pairs must be on the GPU or pinned")
-    dev = next((t.device for _, t in pools if t.device.type == "cuda"), torch.device("cuda"))
+    devs = {t.device for _, t in pools if t.device.type == "cuda"}
+    if src_dst_pairs.device.type == "cuda":
+        devs.add(src_dst_pairs.device)
+    if len(devs) > 1:
+        raise ValueError("all device tensors must be on one GPU")
+    dev = devs.pop() if devs else torch.device("cuda", torch.cuda.current_device())
     nbs, Hkv, bs, hd = src_k.shape
-    rc = _lib.pa_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
-                             src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], nbs, dst_k.shape[0], Hkv, hd, bs,
-                             _dtype_code(src_k.dtype), status.ptr() if status is not None else None,
-                             _stream_ptr(stream, dev))
+    with torch.cuda.device(dev):
+        rc = _lib.pa_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
+                                 src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], nbs, dst_k.shape[0], Hkv, hd,
+                                 bs, _dtype_code(src_k.dtype), status.ptr() if status is not None else None,
+                                 _stream_ptr(stream, dev))
     _raise(rc)
 
 
