@@ -42,15 +42,20 @@ L2_BYTES = 129 * 2**20
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
 # batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
 # attended tokens.  Valid only while the kernel source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "b67df317039bd2b9", "bytes": 919.07e6, "tokens": 219876,
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "c45af64593dec6d9", "bytes": 919.07e6, "tokens": 219876,
                    "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
 
 
 def kernel_source(text: bytes) -> bytes:
-    """The part of pa_decode.cu that the partition pass is compiled from: the
-    includes, device helpers and the bf16/fp32 kernels, up to the reduce kernel."""
+    """The code the partition pass is compiled from: pa_decode.cu up to the
+    reduce kernel (includes, device helpers, the bf16/fp32 kernels), with
+    comments and whitespace removed so that only code changes count."""
+    import re
     cut = text.find(b"// ------------------------------------------------------- split-K reduce ---")
-    return text if cut < 0 else text[:cut]
+    code = text if cut < 0 else text[:cut]
+    code = re.sub(rb"/\*.*?\*/", b"", code, flags=re.S)
+    code = re.sub(rb"//[^\n]*", b"", code)
+    return re.sub(rb"\s+", b" ", code).strip()
 
 
 def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype: str):
@@ -264,6 +269,8 @@ def main():
                     choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the same-run measurement of the GQA Llama-3-70B-shaped batch")
     ap.add_argument("--unfused", action="store_true",
                     help="write the new tokens with a separate pa_reshape_and_cache launch instead of inside "
                          "the decode launch")
@@ -464,6 +471,11 @@ def main():
                          f"all {w.num_q_heads} query heads) of the same workload, fp64 C oracle, "
                          f"{dt:.1f} s"}
 
+    secondary = None
+    if rank == 0 and world == 1 and args.workload == "long_context" and not args.no_secondary:
+        g = measure_step("gqa_llama3_70b", max(args.steps, 100))
+        secondary = {"gqa_llama3_70b": g}
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -515,6 +527,11 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if secondary is not None:
+        for v in secondary.values():
+            v["hbm_fraction"] = round(v["value"] / peak, 4)
+            v["partition_pass_frac"] = round(v["partition_pass_GBps"] / peak, 4)
+        line["secondary_workloads"] = secondary
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -701,6 +718,51 @@ def run_swap_study(args, num_blocks: int = 4096):
                       "contiguous_memcpy_out_GBps": round(nbytes / (mc_out * 1e-3) / 1e9, 1),
                       "contiguous_memcpy_in_GBps": round(nbytes / (mc_in * 1e-3) / 1e9, 1)}),
           flush=True)
+
+
+def measure_step(name: str, steps: int, warmup: int = 5) -> dict:
+    """Graph-replayed decode step (fused cache write + merge) of another
+    workload, timed in the same run: step GB/s and the partition pass alone."""
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    d = build_workload(name, torch.device("cuda", torch.cuda.current_device()), 0)
+    w = d["workload"]
+    e = torch.tensor([], dtype=w.dtype).element_size()
+    B = decode_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e, e)
+    Bp = partition_pass_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e)
+    step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], d["scale"],
+                      d["max_context_len"], w.partition_size)
+    tok = (d["k_new"], d["v_new"], d["slot_mapping"])
+
+    def full(_):
+        step.run_fused(*tok, d["cow_pairs"])
+
+    def part(_):
+        step.decode(None, binding.PA_PHASE_PARTITIONS, *tok)
+
+    for _ in range(warmup):
+        full(None)
+    torch.cuda.synchronize()
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+    stream = torch.cuda.current_stream()
+    out = {}
+    for key, fn in (("step", full), ("partition_pass", part)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn(None)
+        g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[key] = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del d, step
+    torch.cuda.empty_cache()
+    return {"ms_per_step": round(out["step"], 4), "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
+            "partition_pass_GBps": round(Bp / (out["partition_pass"] * 1e-3) / 1e9, 1)}
 
 
 def run_reference(args):

@@ -25,6 +25,9 @@
 // probabilities, split into a bf16 high part and a bf16 residual, feed
 // O += P_hi V + P_lo V directly from registers (two MMAs keep ~16 bits of p).
 // fp32 path: 1-D bulk copies and SIMT fp32 FMAs, one lane per head_dim slice.
+// Fused cache write (optional): the warp whose chunk holds a sequence's new
+// last token copies that row into its staged tile, and the CTA of query-head
+// tile 0 writes it to the caches, so one launch both writes and attends.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
