@@ -298,6 +298,8 @@ def main():
     dist = None
     if world > 1:
         import torch.distributed as dist  # noqa: F811
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
     if args.impl == "reference":
