@@ -468,10 +468,14 @@ def main():
         seqs = pick_sample(d, args.cpu_seconds, threads)
         dt = time_oracle(d, seqs, threads)
         sb = sample_kv_bytes(d, seqs)
+        one = pick_sample(d, min(3.0, args.cpu_seconds), 1)
+        dt1 = time_oracle(d, one, 1)
         cpu = {"value": round(sb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{len(seqs)} of {len(lens)} sequences ({int(sum(lens[s] for s in seqs))} tokens, "
                          f"all {w.num_q_heads} query heads) of the same workload, fp64 C oracle, "
-                         f"{dt:.1f} s"}
+                         f"{dt:.1f} s",
+               "single_core_value": round(sample_kv_bytes(d, one) / dt1 / 1e9, 4),
+               "single_core_sample": f"{len(one)} sequences, 1 thread, {dt1:.1f} s"}
 
     secondary = None
     if rank == 0 and world == 1 and args.workload == "long_context" and not args.no_secondary:
@@ -502,6 +506,7 @@ def main():
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 4),
+        "median_ms_per_step": round(statistics.median(step_ms), 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -529,6 +534,14 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if cow is not None:
+        # prefix sharing: K/V bytes of the distinct blocks the step reads
+        bs = w.block_size
+        tab = d["block_tables"].cpu().numpy()
+        used = {int(b) for i, n in enumerate(lens) for b in tab[i, :-(-int(n) // bs)]}
+        uniq = len(used) * w.num_kv_heads * bs * w.head_dim * 2 * elem
+        line["unique_kv_bytes"] = uniq
+        line["unique_kv_GBps"] = round(uniq / (ms * 1e-3) / 1e9, 1)
     if secondary is not None:
         for v in secondary.values():
             v["hbm_fraction"] = round(v["value"] / peak, 4)
