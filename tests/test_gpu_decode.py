@@ -193,3 +193,22 @@ def test_fused_cache_write_rejects_a_slot_that_is_not_the_last_position(pa):
     assert kc[good // 16, :, good % 16].eq(1).all()                 # sequence 0 written
     plain = run(pa, q, kc, vc, tables, lens_t, 0.1)
     assert torch.equal(_bits(out[1]), _bits(plain[1]))
+
+
+def test_thousands_of_short_sequences(pa):
+    """3000 sequences of 0..300 tokens (many single-partition, some split with
+    P = 128): the warp-parallel walk from work items to sequences stays exact
+    far past one warp's 32 sequences per step."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(0, 301, size=3000).tolist()
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=77, slack=3)
+    status = pa.DeviceStatus()
+    out = run(pa, q, kc, vc, tables, lens_t, 0.1, partition_size=128, status=status)
+    assert status.read() == 0
+    sample = torch.from_numpy(np.stack([np.repeat(np.arange(0, 3000, 7), 2),
+                                        np.tile([0, 15], len(range(0, 3000, 7)))], 1).astype(np.int32))
+    import oracle
+    ref = oracle.paged_decode(q.cpu(), kc.cpu(), vc.cpu(), tables.cpu(), lens_t.cpu(), 0.1, pairs=sample)
+    mask = torch.zeros(q.shape[:2], dtype=torch.bool)
+    mask[sample[:, 0].long(), sample[:, 1].long()] = True
+    assert_decode_close(out, ref, torch.bfloat16, mask=mask, what="3000 sequences")
