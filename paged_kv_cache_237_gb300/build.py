@@ -47,10 +47,24 @@ def _stale(target: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of the shared library."""
+    """Compile (if stale) and return the path of the shared library.  Several
+    processes may call this at once (one per rank): a file lock lets one of
+    them compile while the others wait and then find the library fresh."""
     if not force and not _stale(LIB_PATH):
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    import fcntl
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale(LIB_PATH):
+                return LIB_PATH
+            return _compile(verbose, ptxas_verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile(verbose: bool, ptxas_verbose: bool) -> str:
     nvcc = _nvcc()
     common = ["-std=c++17", "-O3", f"-I{INCLUDE}", f"-I{CSRC}"]
     jobs = []
