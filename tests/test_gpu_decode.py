@@ -212,3 +212,62 @@ def test_thousands_of_short_sequences(pa):
     mask = torch.zeros(q.shape[:2], dtype=torch.bool)
     mask[sample[:, 0].long(), sample[:, 1].long()] = True
     assert_decode_close(out, ref, torch.bfloat16, mask=mask, what="3000 sequences")
+
+
+def test_step_captured_in_a_cuda_graph_replays_bit_identically(pa):
+    """The decode step (fused cache write + both passes) captured once in a
+    CUDA graph and replayed gives the same bits as launching it eagerly."""
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    lens = [40, 700, 1500, 5]
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=41, nan_tails=False)
+    g = torch.Generator().manual_seed(41)
+    kn = torch.randn(4, 2, 128, generator=g).to(torch.bfloat16).cuda()
+    vn = torch.randn(4, 2, 128, generator=g).to(torch.bfloat16).cuda()
+    tab = tables.cpu()
+    slots = torch.tensor([int(tab[i, (n - 1) // 16]) * 16 + (n - 1) % 16 for i, n in enumerate(lens)],
+                         dtype=torch.int64).cuda()
+    step = DecodeStep(q, kc, vc, tables, lens_t, 0.1, max(lens), 256)
+    eager = step.run_fused(kn, vn, slots).clone()
+    torch.cuda.synchronize()
+    step.out.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        step.run_fused(kn, vn, slots)
+    for _ in range(3):
+        step.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(step.out), _bits(eager))
+    assert step.status.read() == 0
+
+
+def test_concurrent_first_calls_from_host_threads(pa):
+    """Several host threads calling pa_decode at once, each on its own stream
+    (the library's per-kernel launch settings are set up under a lock)."""
+    import threading
+    cases = [make_case([300 + 97 * i, 33, 1200], 8, 1, 64 if i % 2 else 128, 16 if i < 2 else 32,
+                       torch.bfloat16, seed=50 + i) for i in range(4)]
+    outs, errors = [None] * 4, []
+
+    def work(i):
+        try:
+            q, kc, vc, tables, lens_t = cases[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                out = torch.empty_like(q)
+                pa.pa_decode(out, q, kc, vc, tables, lens_t, 0.1, max_context_len=int(lens_t.max()),
+                             partition_size=128, stream=s)
+            s.synchronize()
+            outs[i] = out
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, (q, kc, vc, tables, lens_t) in enumerate(cases):
+        ref = oracle_decode(q, kc, vc, tables, lens_t, 0.1)
+        assert_decode_close(outs[i], ref, torch.bfloat16, what=f"thread {i}")
