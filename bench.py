@@ -42,16 +42,16 @@ L2_BYTES = 129 * 2**20
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
 # batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
 # attended tokens.  Valid only while the kernel source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "c45af64593dec6d9", "bytes": 919.07e6, "tokens": 219876,
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "042e83ea9d5030bf", "bytes": 919.07e6, "tokens": 219876,
                    "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
 
 
 def kernel_source(text: bytes) -> bytes:
-    """The code the partition pass is compiled from: pa_decode.cu up to the
-    reduce kernel (includes, device helpers, the bf16/fp32 kernels), with
-    comments and whitespace removed so that only code changes count."""
+    """The code the bf16 partition pass is compiled from: pa_decode.cu up to
+    the SIMT kernel (includes, device helpers, the bf16 kernel), with comments
+    and whitespace removed so that only code changes count."""
     import re
-    cut = text.find(b"// ------------------------------------------------------- split-K reduce ---")
+    cut = text.find(b"// ------------------------------------------------------------ SIMT path ---")
     code = text if cut < 0 else text[:cut]
     code = re.sub(rb"/\*.*?\*/", b"", code, flags=re.S)
     code = re.sub(rb"//[^\n]*", b"", code)
@@ -271,15 +271,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the same-run measurement of the GQA Llama-3-70B-shaped batch")
+    ap.add_argument("--simt", action="store_true",
+                    help="bf16 products on plain fp32 FMAs (SIMT kernel) instead of tensor-core MMAs")
     ap.add_argument("--unfused", action="store_true",
                     help="write the new tokens with a separate pa_reshape_and_cache launch instead of inside "
                          "the decode launch")
-    ap.add_argument("--study", choices=["placement", "prefix_cache", "swap"], default=None,
+    ap.add_argument("--study", choices=["placement", "prefix_cache", "swap", "mma"], default=None,
                     help="instead of the benchmark line, print one study line: 'placement' times the partition "
                          "pass with shuffled vs identity block placement at block sizes 32 and 16; "
                          "'prefix_cache' admits a multi-tenant batch through the chained-key prefix cache and "
                          "times its decode step; 'swap' times block copies between the device cache and pinned "
-                         "host memory")
+                         "host memory; 'mma' times the bf16 partition pass on tensor-core MMAs vs SIMT FMAs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.study == "placement":
@@ -290,6 +292,9 @@ def main():
         return
     if args.study == "swap":
         run_swap_study(args)
+        return
+    if args.study == "mma":
+        run_mma_study(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -323,7 +328,7 @@ def main():
     B = decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, elem, elem, elem)
     B_part = partition_pass_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, elem, elem)
     step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], d["scale"],
-                      d["max_context_len"], w.partition_size)
+                      d["max_context_len"], w.partition_size, simt=args.simt)
     split = binding.pa_decode_workspace_size(len(lens), w.num_q_heads, w.head_dim, d["max_context_len"],
                                              w.partition_size) > 0
     stream = torch.cuda.current_stream(device)
@@ -521,13 +526,14 @@ def main():
         "eager_ms_per_step": round(eager_ms, 4),
         "phases_ms": {"cache_updates": round(statistics.mean(write_ms), 4),
                       "partition_pass": round(part_avg, 4), "split_k_reduce": round(statistics.mean(red_ms), 4)},
-        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)" if w.dtype == torch.bfloat16
-                     else "decode_f32_kernel (partition pass)",
+        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)"
+                     if w.dtype == torch.bfloat16 and not args.simt else "decode_simt_kernel (partition pass)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "bytes_per_launch": B_part,
-                     "traffic": captured_traffic(int(sum(int(n) for n in lens)), w.num_kv_heads, w.head_dim,
-                                                 "bf16" if w.dtype == torch.bfloat16 else "f32")},
+                     "traffic": None if args.simt else captured_traffic(
+                         int(sum(int(n) for n in lens)), w.num_kv_heads, w.head_dim,
+                         "bf16" if w.dtype == torch.bfloat16 else "f32")},
         "e2e": {"value": round(B_job / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
@@ -778,6 +784,58 @@ def measure_step(name: str, steps: int, warmup: int = 5) -> dict:
     torch.cuda.empty_cache()
     return {"ms_per_step": round(out["step"], 4), "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
             "partition_pass_GBps": round(Bp / (out["partition_pass"] * 1e-3) / 1e9, 1)}
+
+
+def run_mma_study(args):
+    """Does batching the query-head group into mma tiles pay off?  The bf16
+    partition pass with its products on tensor-core MMAs (the default) and on
+    plain fp32 FMAs (SIMT kernel), same inputs, CUDA graphs, per workload."""
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    rows = {}
+    for name in ("mha_llama2_7b", "gqa_llama3_70b", "long_context"):
+        d = build_workload(name, dev, 0)
+        w = d["workload"]
+        Bp = partition_pass_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, 2, 2)
+        row = {"group": w.num_q_heads // w.num_kv_heads}
+        outs = {}
+        for mode, simt in (("mma", False), ("simt", True)):
+            step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                              d["scale"], d["max_context_len"], w.partition_size, simt=simt)
+            for _ in range(args.warmup):
+                step.decode(None, binding.PA_PHASE_PARTITIONS)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                step.decode(None, binding.PA_PHASE_PARTITIONS)
+            g.replay()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for a, b in ev:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+            step.decode(None, binding.PA_PHASE_ALL)
+            torch.cuda.synchronize()
+            if step.status.read():
+                raise RuntimeError("device status flagged an input error")
+            outs[mode] = step.out.float().clone()
+            row[f"{mode}_ms"] = round(ms, 4)
+            row[f"{mode}_GBps"] = round(Bp / (ms * 1e-3) / 1e9, 1)
+            del step
+        row["simt_over_mma_time"] = round(row["simt_ms"] / row["mma_ms"], 3)
+        row["max_abs_diff_mma_vs_simt"] = float((outs["mma"] - outs["simt"]).abs().max())
+        rows[name] = row
+        del d
+        torch.cuda.empty_cache()
+    print(json.dumps({"study": "mma", "kernel": "partition pass", "steps": args.steps, "results": rows}), flush=True)
 
 
 def run_reference(args):

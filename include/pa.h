@@ -122,6 +122,12 @@ typedef struct pa_decode_args {
     const void *k_new;
     const void *v_new;
     const int64_t *slot_mapping;
+    int simt;               /* PA_BF16 only: nonzero computes q.K and p.V with
+                               plain fp32 FMAs (p kept in fp32, 8 query heads
+                               per work item) instead of tensor-core MMAs;
+                               0, the default, uses the MMAs.  Same results
+                               within the tolerance; for comparison and for
+                               callers who want fp32 products throughout. */
 } pa_decode_args;
 
 #define PA_PHASE_ALL 0

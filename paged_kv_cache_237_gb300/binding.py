@@ -60,6 +60,7 @@ class _DecodeArgs(ctypes.Structure):
         ("k_new", ctypes.c_void_p),
         ("v_new", ctypes.c_void_p),
         ("slot_mapping", ctypes.c_void_p),
+        ("simt", ctypes.c_int),
     ]
 
 
@@ -202,7 +203,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
               max_context_len: int, partition_size: int = 0, workspace: torch.Tensor | None = None,
               status: DeviceStatus | None = None, stream=None, phase: int = 0,
               k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
-              slot_mapping: torch.Tensor | None = None) -> torch.Tensor:
+              slot_mapping: torch.Tensor | None = None, simt: bool = False) -> torch.Tensor:
     """Paged decode attention; writes ``out`` [S, Hq, hd] and returns it.
 
     q [S, Hq, hd]; k_cache, v_cache [num_blocks, Hkv, block_size, hd];
@@ -213,7 +214,8 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
 
     With k_new, v_new [S, Hkv, hd] and slot_mapping [S] int64, each
     sequence's new (last) token is written into the caches and attended in the
-    same launch (fused cache write).
+    same launch (fused cache write).  ``simt=True`` (bf16 only) computes the
+    products with fp32 FMAs instead of tensor-core MMAs.
     """
     fdt = (torch.float32, torch.bfloat16)
     _check_cuda(q, "q", fdt)
@@ -253,7 +255,8 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
                        _stream_ptr(stream, dev), phase,
                        k_new.data_ptr() if k_new is not None else None,
                        v_new.data_ptr() if v_new is not None else None,
-                       slot_mapping.data_ptr() if slot_mapping is not None else None)
+                       slot_mapping.data_ptr() if slot_mapping is not None else None,
+                       1 if simt else 0)
     with torch.cuda.device(dev):
         rc = _lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                             block_tables.data_ptr(), context_lens.data_ptr(), Hq, Hkv, hd, bs,

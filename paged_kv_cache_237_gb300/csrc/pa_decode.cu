@@ -24,7 +24,8 @@
 // the M dimension of mma.m16n8k16: S = Q K^T (tokens are N), then the fp32
 // probabilities, split into a bf16 high part and a bf16 residual, feed
 // O += P_hi V + P_lo V directly from registers (two MMAs keep ~16 bits of p).
-// fp32 path: 1-D bulk copies and SIMT fp32 FMAs, one lane per head_dim slice.
+// SIMT path (fp32 inputs, or bf16 on request): 1-D bulk copies and fp32 FMAs,
+// one lane per head_dim slice.
 // Fused cache write (optional): the warp whose chunk holds a sequence's new
 // last token copies that row into its staged tile, and the CTA of query-head
 // tile 0 writes it to the caches, so one launch both writes and attends.
@@ -500,12 +501,45 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
-// ------------------------------------------------------------ fp32 path ---
-template <int HD, int NSTAGE>
-__global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodeParams p) {
+// ------------------------------------------------------------ SIMT path ---
+// fp32 inputs, and bf16 inputs when the caller asks for it: plain fp32 FMAs,
+// one lane per head_dim slice, p kept in fp32.  Elements are widened to fp32 as
+// they are read from the staged tiles.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// VEC consecutive elements of one staged row, widened to fp32.
+template <int VEC>
+__device__ __forceinline__ void load_row(const float *src, float (&dst)[VEC]) {
+    if constexpr (VEC == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        dst[0] = v.x, dst[1] = v.y, dst[2] = v.z, dst[3] = v.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) dst[i] = src[i];
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *src, float (&dst)[VEC]) {
+    if constexpr (VEC == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(src);
+        __nv_bfloat162 a, b;
+        memcpy(&a, &raw.x, 4);
+        memcpy(&b, &raw.y, 4);
+        const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+        dst[0] = fa.x, dst[1] = fa.y, dst[2] = fb.x, dst[3] = fb.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) dst[i] = __bfloat162float(src[i]);
+    }
+}
+
+template <typename T, int HD, int NSTAGE>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_simt_kernel(const DecodeParams p) {
     constexpr int VEC = HD / 32;                 // head_dim elements per lane
     constexpr int HT = 8;                        // query heads per tile
-    constexpr int PAGE_BYTES = kChunk * HD * 4;
+    constexpr int PAGE_BYTES = kChunk * HD * static_cast<int>(sizeof(T));
     constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
     constexpr int WARP_BYTES = NSTAGE * STAGE_BYTES;
     constexpr int LD = HD + kEpiPad;
@@ -547,7 +581,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
                 // An invalid block id completes the stage with no data (flagged).
                 mbar_arrive_expect_tx(bar, row >= 0 ? STAGE_BYTES : 0);
                 if (row >= 0) {
-                    const long long off = (long long)row * HD * 4;
+                    const long long off = (long long)row * HD * static_cast<long long>(sizeof(T));
                     bulk_load(dst, kc + off, PAGE_BYTES, bar);
                     bulk_load(dst + PAGE_BYTES, vc + off, PAGE_BYTES, bar);
                 }
@@ -557,12 +591,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
 
         float q[HT][VEC];
         {
-            const float *qb = static_cast<const float *>(p.q) +
-                              ((long long)it.seq * p.num_q_heads + it.qh0) * HD + lane * VEC;
+            const T *qb = static_cast<const T *>(p.q) +
+                          ((long long)it.seq * p.num_q_heads + it.qh0) * HD + lane * VEC;
 #pragma unroll
             for (int h = 0; h < HT; ++h)
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) q[h][v] = h < it.rows ? qb[h * HD + v] : 0.f;
+                for (int v = 0; v < VEC; ++v) q[h][v] = h < it.rows ? to_f32(qb[h * HD + v]) : 0.f;
         }
         const int pro = my_n < NSTAGE ? my_n : NSTAGE;
         for (int k = 0; k < pro; ++k) issue(k);
@@ -587,35 +621,32 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
                 break;
             }
             ++n_done;
-            const float *Ks = reinterpret_cast<const float *>(wbuf + s * STAGE_BYTES);
-            const float *Vs = Ks + kChunk * HD;
+            const T *Ks = reinterpret_cast<const T *>(wbuf + s * STAGE_BYTES);
+            const T *Vs = Ks + kChunk * HD;
             const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
             const int valid = min(kChunk, it.tok_end - tok0);
             if (warp + kWarps * k == ntok.chunk) {
                 // Fused cache write (see the bf16 kernel); plain row layout here.
-                constexpr int V4 = HD / 4;
-                const long long src = ((long long)it.seq * p.num_kv_heads + it.kvh) * V4;
-                const float4 *kn = static_cast<const float4 *>(p.k_new) + src;
-                const float4 *vn = static_cast<const float4 *>(p.v_new) + src;
-                float4 *st = reinterpret_cast<float4 *>(wbuf + s * STAGE_BYTES);
-                for (int i = lane; i < 2 * V4; i += 32) {
-                    const bool isv = i >= V4;
-                    const int c = isv ? i - V4 : i;
-                    const float4 val = isv ? vn[c] : kn[c];
-                    st[(isv ? kChunk * V4 : 0) + ntok.row * V4 + c] = val;
+                constexpr int V16 = HD * static_cast<int>(sizeof(T)) / 16;   // 16-byte pieces per row
+                const long long src = ((long long)it.seq * p.num_kv_heads + it.kvh) * V16;
+                const uint4 *kn = static_cast<const uint4 *>(p.k_new) + src;
+                const uint4 *vn = static_cast<const uint4 *>(p.v_new) + src;
+                uint4 *st = reinterpret_cast<uint4 *>(wbuf + s * STAGE_BYTES);
+                for (int i = lane; i < 2 * V16; i += 32) {
+                    const bool isv = i >= V16;
+                    const int c = isv ? i - V16 : i;
+                    const uint4 val = isv ? vn[c] : kn[c];
+                    st[(isv ? kChunk * V16 : 0) + ntok.row * V16 + c] = val;
                     if (it.ht == 0)
-                        static_cast<float4 *>(isv ? p.v_cache_w : p.k_cache_w)[ntok.cache_row * V4 + c] = val;
+                        static_cast<uint4 *>(isv ? p.v_cache_w : p.k_cache_w)[ntok.cache_row * V16 + c] = val;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
             for (int tt = 0; tt < valid; ++tt) {
                 float kv[VEC], vv[VEC];
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) {
-                    kv[v] = Ks[tt * HD + lane * VEC + v];
-                    vv[v] = Vs[tt * HD + lane * VEC + v];
-                }
+                load_row<VEC>(Ks + tt * HD + lane * VEC, kv);
+                load_row<VEC>(Vs + tt * HD + lane * VEC, vv);
 #pragma unroll
                 for (int h = 0; h < HT; ++h) {
                     if (h < it.rows) {
@@ -654,7 +685,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_f32_kernel(const DecodePar
             }
         }
         __syncthreads();
-        merge_and_store<float, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows, it.single);
+        merge_and_store<T, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows, it.single);
         fence_proxy_async_smem();
         __syncthreads();
     }
@@ -813,8 +844,8 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
 
 template <int HD>
 constexpr int bf16_stages() { return HD == 128 ? 3 : 4; }
-template <int HD>
-constexpr int f32_stages() { return 2; }
+template <typename T>
+constexpr int simt_stages() { return sizeof(T) == 4 ? 2 : 3; }
 
 template <int HD, bool ROWS16>
 int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache, long long items,
@@ -835,14 +866,14 @@ int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache,
     return PA_OK;
 }
 
-template <int HD>
-int launch_f32(const DecodeParams &p, long long items, int dev, cudaStream_t st) {
-    constexpr int NS = f32_stages<HD>();
-    constexpr int SMEM = pa::kWarps * NS * 2 * pa::kChunk * HD * 4 + pa::kWarps * NS * 8 + 1024;
+template <typename T, int HD>
+int launch_simt(const DecodeParams &p, long long items, int dev, cudaStream_t st) {
+    constexpr int NS = simt_stages<T>();
+    constexpr int SMEM = pa::kWarps * NS * 2 * pa::kChunk * HD * static_cast<int>(sizeof(T)) + pa::kWarps * NS * 8 + 1024;
     static KernelSlot slot;
-    auto kernel = pa::decode_f32_kernel<HD, NS>;
+    auto kernel = pa::decode_simt_kernel<T, HD, NS>;
     const int occ = ensure_kernel(kernel, slot, SMEM, dev);
-    if (occ == 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot configure the fp32 kernel");
+    if (occ == 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot configure the SIMT kernel");
     const long long cap = static_cast<long long>(sm_count(dev)) * occ;
     const int grid = static_cast<int>(items < cap ? items : cap);
     kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(p);
@@ -940,7 +971,8 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     p.ctx_cap = ctx_cap;
     p.total_rows = static_cast<int>(total_rows);
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int tile = a->dtype == PA_BF16 ? 16 : 8;
+    const bool use_mma = a->dtype == PA_BF16 && !a->simt;
+    const int tile = use_mma ? 16 : 8;
     p.tile_rows = p.group < tile ? p.group : tile;
     p.head_tiles = (p.group + tile - 1) / tile;
 
@@ -953,7 +985,7 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     int rc = PA_OK;
     if (a->phase == PA_PHASE_REDUCE) {
         // only the merge pass below
-    } else if (a->dtype == PA_BF16) {
+    } else if (use_mma) {
         const bool rows16 = p.group > 8;
         if (head_dim == 128)
             rc = rows16 ? launch_bf16<128, true>(p, k_cache, v_cache, items, dev, st)
@@ -962,7 +994,12 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
             rc = rows16 ? launch_bf16<64, true>(p, k_cache, v_cache, items, dev, st)
                         : launch_bf16<64, false>(p, k_cache, v_cache, items, dev, st);
     } else {
-        rc = head_dim == 128 ? launch_f32<128>(p, items, dev, st) : launch_f32<64>(p, items, dev, st);
+        if (a->dtype == PA_BF16)
+            rc = head_dim == 128 ? launch_simt<__nv_bfloat16, 128>(p, items, dev, st)
+                                 : launch_simt<__nv_bfloat16, 64>(p, items, dev, st);
+        else
+            rc = head_dim == 128 ? launch_simt<float, 128>(p, items, dev, st)
+                                 : launch_simt<float, 64>(p, items, dev, st);
     }
     if (rc != PA_OK) return rc;
     if (max_parts > 1 && a->phase != PA_PHASE_PARTITIONS) {

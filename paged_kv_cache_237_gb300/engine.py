@@ -22,12 +22,13 @@ class DecodeStep:
 
     def __init__(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
-                 max_context_len: int, partition_size: int = 0):
+                 max_context_len: int, partition_size: int = 0, simt: bool = False):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.scale = scale
         self.max_context_len = max_context_len
         self.partition_size = partition_size
+        self.simt = simt
         self.out = torch.empty_like(q)
         S, Hq, hd = q.shape
         ws = binding.pa_decode_workspace_size(S, Hq, hd, max_context_len, partition_size)
@@ -40,7 +41,7 @@ class DecodeStep:
                                  self.context_lens, self.scale, max_context_len=self.max_context_len,
                                  partition_size=self.partition_size, workspace=self.workspace,
                                  status=self.status, stream=stream, phase=phase, k_new=k_new,
-                                 v_new=v_new, slot_mapping=slot_mapping)
+                                 v_new=v_new, slot_mapping=slot_mapping, simt=self.simt)
 
     def run_fused(self, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                   cow_pairs: torch.Tensor | None = None, stream=None,

@@ -29,15 +29,18 @@ def run(pa, q, kc, vc, tables, lens, scale, partition_size=0, status=None, max_c
     return out
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype,simt", [(torch.bfloat16, False), (torch.bfloat16, True), (torch.float32, False)])
 @pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (16, 2), (16, 1), (12, 4), (40, 2)])
-def test_edge_lengths_match_oracle(pa, dtype, hd, bs, Hq, Hkv):
+def test_edge_lengths_match_oracle(pa, dtype, simt, hd, bs, Hq, Hkv):
     q, kc, vc, tables, lens = make_case(EDGE_LENS, Hq, Hkv, hd, bs, dtype, seed=hd + bs + Hq)
     scale = 1.0 / math.sqrt(hd)
     status = pa.DeviceStatus()
-    out = run(pa, q, kc, vc, tables, lens, scale, status=status)
+    out = torch.empty_like(q)
+    pa.pa_decode(out, q, kc, vc, tables, lens, scale, max_context_len=int(lens.max().item()), status=status,
+                 simt=simt)
+    torch.cuda.synchronize()
     assert status.read() == 0
     ref = oracle_decode(q, kc, vc, tables, lens, scale)
     assert_decode_close(out, ref, dtype, what=f"{dtype} hd{hd} bs{bs} {Hq}/{Hkv}")
@@ -142,9 +145,9 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype,simt", [(torch.bfloat16, False), (torch.bfloat16, True), (torch.float32, False)])
 @pytest.mark.parametrize("hd,bs,Hq,Hkv", [(128, 16, 8, 1), (64, 32, 40, 2), (128, 32, 32, 8)])
-def test_fused_cache_write_matches_write_then_decode(pa, dtype, hd, bs, Hq, Hkv):
+def test_fused_cache_write_matches_write_then_decode(pa, dtype, simt, hd, bs, Hq, Hkv):
     """One launch that writes each sequence's new token and attends with it gives
     bit-identical outputs and caches to pa_reshape_and_cache then pa_decode.
     Sequence 2 is padding (slot -1): neither path writes it."""
@@ -161,11 +164,13 @@ def test_fused_cache_write_matches_write_then_decode(pa, dtype, hd, bs, Hq, Hkv)
     slots = slots.cuda()
     kc_a, vc_a = kc.clone(), vc.clone()
     pa.pa_reshape_and_cache(k_new, v_new, kc_a, vc_a, slots)
-    out_a = run(pa, q, kc_a, vc_a, tables, lens_t, 0.1, partition_size=256)
+    out_a = torch.empty_like(q)
+    pa.pa_decode(out_a, q, kc_a, vc_a, tables, lens_t, 0.1, max_context_len=max(lens), partition_size=256,
+                 simt=simt)
     status = pa.DeviceStatus()
     out_b = torch.empty_like(q)
     pa.pa_decode(out_b, q, kc, vc, tables, lens_t, 0.1, max_context_len=max(lens), partition_size=256,
-                 status=status, k_new=k_new, v_new=v_new, slot_mapping=slots)
+                 status=status, k_new=k_new, v_new=v_new, slot_mapping=slots, simt=simt)
     torch.cuda.synchronize()
     assert status.read() == 0
     assert torch.equal(_bits(out_a), _bits(out_b))

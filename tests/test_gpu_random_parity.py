@@ -1,7 +1,7 @@
 """Seeded random sweep of pa_decode configurations against the fp64 oracle:
 dtype, head_dim, block size, group size (1..40, several head tiles), partition
 size, lengths (0, 1, block edges, long), block placement, NaN tails, fused or
-separate cache write.  Every case must meet the tolerance and leave the
+separate cache write, tensor-core or SIMT products for bf16.  Every case must meet the tolerance and leave the
 status word clear."""
 import math
 
@@ -39,13 +39,14 @@ def draw(rng):
         else:
             lens.append(int(rng.integers(1, 3000)))
     fused = bool(rng.random() < 0.5)
-    return dtype, hd, bs, Hkv, group * Hkv, P, lens, fused
+    simt = dtype == torch.bfloat16 and bool(rng.random() < 0.3)
+    return dtype, hd, bs, Hkv, group * Hkv, P, lens, fused, simt
 
 
 @pytest.mark.parametrize("seed", range(40))
 def test_random_configuration_matches_oracle(pa, seed):
     rng = np.random.default_rng(1000 + seed)
-    dtype, hd, bs, Hkv, Hq, P, lens, fused = draw(rng)
+    dtype, hd, bs, Hkv, Hq, P, lens, fused, simt = draw(rng)
     q, kc, vc, tables, lens_t = make_case(lens, Hq, Hkv, hd, bs, dtype, seed=seed, slack=int(rng.integers(0, 9)))
     scale = float(rng.uniform(0.02, 0.2)) if rng.random() < 0.9 else 1.0 / math.sqrt(hd)
     max_ctx = max(lens) if max(lens) > 0 else 1
@@ -62,15 +63,15 @@ def test_random_configuration_matches_oracle(pa, seed):
         kc_ref, vc_ref = kc.cpu(), vc.cpu()
         oracle.reshape_and_cache(k_new, v_new, kc_ref, vc_ref, slots)
         pa.pa_decode(out, q, kc, vc, tables, lens_t, scale, max_context_len=max_ctx, partition_size=P,
-                     status=status, k_new=k_new.cuda(), v_new=v_new.cuda(), slot_mapping=slots.cuda())
+                     status=status, k_new=k_new.cuda(), v_new=v_new.cuda(), slot_mapping=slots.cuda(), simt=simt)
         torch.cuda.synchronize()
         assert torch.equal(kc.cpu().view(torch.uint8), kc_ref.view(torch.uint8))
     else:
         kc_ref, vc_ref = kc, vc
         pa.pa_decode(out, q, kc, vc, tables, lens_t, scale, max_context_len=max_ctx, partition_size=P,
-                     status=status)
+                     status=status, simt=simt)
         torch.cuda.synchronize()
     assert status.read() == 0
     ref = oracle_decode(q, kc_ref, vc_ref, tables, lens_t, scale)
     assert_decode_close(out, ref, dtype,
-                        what=f"seed {seed}: {dtype} hd{hd} bs{bs} {Hq}/{Hkv} P={P} lens={lens} fused={fused}")
+                        what=f"seed {seed}: {dtype} hd{hd} bs{bs} {Hq}/{Hkv} P={P} lens={lens} fused={fused} simt={simt}")
