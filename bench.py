@@ -38,12 +38,15 @@ import torch  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); seq-layer decode steps/s"
 L2_BYTES = 129 * 2**20
 
-# DRAM read+write bytes of one partition-pass launch from a single ncu capture
-# (profiles/decode_bf16_kernel_gqa_llama3_70b.md), taken on a 219,876-token GQA
-# batch (8 KV heads, head_dim 128, bf16) and scaled to the benchmarked launch by
-# attended tokens.  Valid only while the kernel source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "042e83ea9d5030bf", "bytes": 919.07e6, "tokens": 219876,
-                   "num_kv_heads": 8, "head_dim": 128, "dtype": "bf16"}
+# DRAM read+write bytes of one partition-pass launch (with the fused cache
+# write), per workload, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
+# (a one-pass capture) of that workload's own launch: the long-context launch at
+# full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
+# (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
+# source is the one captured.
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "8d243d7b05097e66",
+                   "bytes_per_launch": {"long_context": 20.80e9 + 293.94e6,
+                                        "gqa_llama3_70b": 902.33e6 + 6.27e6}}
 
 
 def kernel_source(text: bytes) -> bytes:
@@ -58,7 +61,9 @@ def kernel_source(text: bytes) -> bytes:
     return re.sub(rb"\s+", b" ", code).strip()
 
 
-def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype: str):
+def captured_traffic(workload: str):
+    """Measured DRAM bytes of one partition-pass launch of `workload`, or None
+    when there is no capture of it or the kernel changed since."""
     import hashlib
     src = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc", "pa_decode.cu")
     try:
@@ -67,10 +72,9 @@ def captured_traffic(total_tokens: int, num_kv_heads: int, head_dim: int, dtype:
     except OSError:
         return None
     c = TRAFFIC_CAPTURE
-    if (digest != c["source_sha256_prefix"] or num_kv_heads != c["num_kv_heads"] or head_dim != c["head_dim"]
-            or dtype != c["dtype"]):
+    if digest != c["source_sha256_prefix"] or workload not in c["bytes_per_launch"]:
         return None
-    return int(c["bytes"] * total_tokens / c["tokens"])
+    return int(c["bytes_per_launch"][workload])
 
 
 # ------------------------------------------------------------ accounting ---
@@ -561,9 +565,7 @@ def main():
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "bytes_per_launch": B_part,
-                     "traffic": None if args.simt else captured_traffic(
-                         int(sum(int(n) for n in lens)), w.num_kv_heads, w.head_dim,
-                         "bf16" if w.dtype == torch.bfloat16 else "f32")},
+                     "traffic": None if args.simt or args.unfused else captured_traffic(w.name)},
         "e2e": {"value": round(B_job / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "public Python API; pinned host inputs copied and output read back every step, "

@@ -20,8 +20,10 @@
 //
 // bf16 path: each 16-token chunk of K and V arrives as 2-D TMA boxes of
 // 16 rows x 64 elements with the 128-byte swizzle, which makes the ldmatrix
-// reads below bank-conflict free.  The query-head group (up to 16 heads) is
-// the M dimension of mma.m16n8k16: S = Q K^T (tokens are N), then the fp32
+// reads below bank-conflict free.  The boxes are loaded under an L2
+// evict-first policy: each K/V row is read once per step, and the split-K
+// partials written meanwhile then stay in L2.  The query-head group (up to 16
+// heads) is the M dimension of mma.m16n8k16: S = Q K^T (tokens are N), the fp32
 // probabilities, split into a bf16 high part and a bf16 residual, feed
 // O += P_hi V + P_lo V directly from registers (two MMAs keep ~16 bits of p).
 // SIMT path (fp32 inputs, or bf16 on request): 1-D bulk copies and fp32 FMAs,
@@ -254,6 +256,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     bool failed = false;
     SeqCursor cur{0, 0};
     const int oob_row = p.total_rows;
+    const uint64_t kv_policy = l2_evict_first_policy();
 
     for (long long item = blockIdx.x;; item += gridDim.x) {
         Item it;
@@ -281,8 +284,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                    tma_load_2d(dst + h * HALF_BYTES, &tmK, h * 64, row, bar);
-                    tma_load_2d(dst + PAGE_BYTES + h * HALF_BYTES, &tmV, h * 64, row, bar);
+                    tma_load_2d_hint(dst + h * HALF_BYTES, &tmK, h * 64, row, bar, kv_policy);
+                    tma_load_2d_hint(dst + PAGE_BYTES + h * HALF_BYTES, &tmV, h * 64, row, bar, kv_policy);
                 }
             }
             ++n_issued;
