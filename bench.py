@@ -44,9 +44,9 @@ L2_BYTES = 129 * 2**20
 # full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
 # source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "8d243d7b05097e66",
-                   "bytes_per_launch": {"long_context": 20.80e9 + 293.94e6,
-                                        "gqa_llama3_70b": 902.33e6 + 6.27e6}}
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "1fa091a52640c95c",
+                   "bytes_per_launch": {"long_context": 20802785280 + 295916800,
+                                        "gqa_llama3_70b": 902333184 + 6208512}}
 
 
 def kernel_source(text: bytes) -> bytes:
@@ -86,6 +86,15 @@ def decode_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem,
     qo = len(lens) * num_q_heads * head_dim * (q_elem + out_elem)
     tables = sum(-(-n // block_size) for n in lens) * 4
     return kv + qo + tables + 4 * len(lens)
+
+
+def decode_bytes_pages(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem, out_elem):
+    """decode_bytes with K/V counted by whole pages: every used block's
+    block_size rows, so a partial last block counts in full (secondary)."""
+    lens = [int(n) for n in lens]
+    pages = sum(-(-n // block_size) for n in lens)
+    return (decode_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem, out_elem)
+            + (pages * block_size - sum(lens)) * num_kv_heads * head_dim * 2 * kv_elem)
 
 
 def partition_pass_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, kv_elem, q_elem):
@@ -147,7 +156,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- workloads ---
-def build_workload(name: str, device, seed_offset: int):
+def build_workload(name: str, device, seed_offset: int, gqa_sigma: float = 1.0):
     from paged_kv_cache_237_gb300 import engine, workloads
     if name == "prefix_share":
         st = engine.prefix_share_state(device, seed=workloads.WORKLOADS[name].seed + seed_offset)
@@ -158,7 +167,8 @@ def build_workload(name: str, device, seed_offset: int):
                  cow_pairs=st["pairs"].to(device), lens=st["lens"].numpy(), scale=st["scale"],
                  max_context_len=st["max_context_len"])
     else:
-        d = workloads.decode_inputs(name, device=device, seed=workloads.WORKLOADS[name].seed + seed_offset)
+        d = workloads.decode_inputs(name, device=device, seed=workloads.WORKLOADS[name].seed + seed_offset,
+                                    gqa_sigma=gqa_sigma)
         d["cow_pairs"] = None
     return d
 
@@ -175,13 +185,14 @@ def combine_ranks(ms_local: float, bytes_local: int, dist=None, device="cpu"):
     return float(t.item()), int(b.item())
 
 
-def workload_config(w, d, world: int) -> dict:
+def workload_config(w, d, world: int, gqa_sigma: float = 1.0) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     lens = d["lens"]
     elem = torch.tensor([], dtype=w.dtype).element_size()
     working_set = d["k_cache"].numel() * elem * 2
+    extra = {"lognormal_sigma": gqa_sigma} if w.name == "gqa_llama3_70b" else {}
     return {
-        "workload": w.name,
+        "workload": w.name, **extra,
         "num_seqs": len(lens), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
         "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": w.partition_size,
         "total_context_tokens": int(sum(int(n) for n in lens)),
@@ -271,6 +282,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_context",
                     choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
+    ap.add_argument("--gqa-sigma", type=float, default=1.0,
+                    help="log-space spread of the GQA batch's lognormal lengths (1.0; 0.5 is the sensitivity case)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
@@ -325,7 +338,7 @@ def main():
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    d = build_workload(args.workload, device, seed_offset=rank)
+    d = build_workload(args.workload, device, seed_offset=rank, gqa_sigma=args.gqa_sigma)
     w = d["workload"]
     elem = torch.tensor([], dtype=w.dtype).element_size()
     lens = d["lens"]
@@ -426,6 +439,8 @@ def main():
     torch.cuda.synchronize(device)
     eager_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms, B_job = combine_ranks(statistics.mean(step_ms), B, dist, device)
+    _, B_pages = combine_ranks(ms, decode_bytes_pages(lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                      w.block_size, elem, elem, elem), dist, device)
     launches_per_step = (0 if fused or not d["slot_mapping"].numel() else 1) + 1 + (1 if split else 0) + \
         (1 if cow is not None and cow.numel() else 0)
 
@@ -448,15 +463,16 @@ def main():
     d2h = houts[0].numel() * houts[0].element_size()
     sets = []
     for j in range(2):
+        # steps run one after another on one stream: they share the workspace and status word
         sj = DecodeStep(torch.empty_like(d["q"]), d["k_cache"], d["v_cache"], torch.empty_like(d["block_tables"]),
                         torch.empty_like(d["context_lens"]), d["scale"], d["max_context_len"], w.partition_size,
-                        simt=args.simt)
-        sj.workspace, sj.status = step.workspace, step.status      # steps run one after another: share
+                        simt=args.simt, workspace=step.workspace, status=step.status)
         sets.append(dict(step=sj, k=torch.empty_like(d["k_new"]), v=torch.empty_like(d["v_new"]),
                          slots=torch.empty_like(d["slot_mapping"]),
                          cow=torch.empty_like(cow) if hcow is not None else None,
                          in_ready=torch.cuda.Event(), done=torch.cuda.Event()))
     copy_stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)      # nothing allocated above is still being written by another stream
 
     def h2d_inputs(bs):
         st = bs["step"]
@@ -518,8 +534,9 @@ def main():
 
     secondary = None
     if rank == 0 and world == 1 and args.workload == "long_context" and not args.no_secondary:
-        g = measure_step("gqa_llama3_70b", max(args.steps, 100))
-        secondary = {"gqa_llama3_70b": g}
+        n2 = max(args.steps, 100)
+        secondary = {"gqa_llama3_70b": measure_step("gqa_llama3_70b", n2),
+                     "gqa_llama3_70b_sigma0.5": measure_step("gqa_llama3_70b", n2, gqa_sigma=0.5)}
 
     if rank != 0:
         if dist is not None:
@@ -551,8 +568,10 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
-        "config": workload_config(w, d, world),
+        "config": workload_config(w, d, world, args.gqa_sigma),
         "hbm_fraction": round(B / (ms * 1e-3) / 1e9 / peak, 4),
+        "page_granular": {"bytes_per_step": B_pages, "GBps": round(B_pages / (ms * 1e-3) / 1e9, 2),
+                          "what": "K/V counted by whole pages (partial last blocks in full)"},
         "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
         "step": "copy-on-write copies + decode launch that also writes the new tokens + split-K merge" if fused
                 else "copy-on-write copies + cache write + decode + split-K merge",
@@ -775,12 +794,12 @@ def run_swap_study(args, num_blocks: int = 4096):
           flush=True)
 
 
-def measure_step(name: str, steps: int, warmup: int = 5) -> dict:
+def measure_step(name: str, steps: int, warmup: int = 5, gqa_sigma: float = 1.0) -> dict:
     """Graph-replayed decode step (fused cache write + merge) of another
     workload, timed in the same run: step GB/s and the partition pass alone."""
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.engine import DecodeStep
-    d = build_workload(name, torch.device("cuda", torch.cuda.current_device()), 0)
+    d = build_workload(name, torch.device("cuda", torch.cuda.current_device()), 0, gqa_sigma)
     w = d["workload"]
     e = torch.tensor([], dtype=w.dtype).element_size()
     B = decode_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e, e)
@@ -814,10 +833,15 @@ def measure_step(name: str, steps: int, warmup: int = 5) -> dict:
             b.record(stream)
         torch.cuda.synchronize()
         out[key] = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tokens = int(sum(int(n) for n in d["lens"]))
     del d, step
     torch.cuda.empty_cache()
-    return {"ms_per_step": round(out["step"], 4), "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
-            "partition_pass_GBps": round(Bp / (out["partition_pass"] * 1e-3) / 1e9, 1)}
+    res = {"ms_per_step": round(out["step"], 4), "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
+           "partition_pass_GBps": round(Bp / (out["partition_pass"] * 1e-3) / 1e9, 1),
+           "total_context_tokens": tokens}
+    if name == "gqa_llama3_70b":
+        res["lognormal_sigma"] = gqa_sigma
+    return res
 
 
 def run_mma_study(args):
@@ -886,7 +910,7 @@ def run_reference(args):
         return
     # Build the workload on the GPU when there is one (same generator as our arm), else on the host.
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    d = workloads.decode_inputs(name, device=device)
+    d = workloads.decode_inputs(name, device=device, gqa_sigma=args.gqa_sigma)
     threads = host_cores()
     per_step = max(0.5, min(10.0, 150.0 / (args.steps + args.warmup)))
     seqs = pick_sample(d, per_step, threads)
@@ -909,7 +933,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, d, 1),
+        "config": workload_config(w, d, 1, args.gqa_sigma),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

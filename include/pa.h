@@ -85,9 +85,13 @@ extern "C" {
  *
  * Long contexts are cut into partitions of `partition_size` tokens that are
  * processed independently and merged by a second pass (split-K), which needs
- * `workspace`.  Arithmetic: fp32 accumulation; for PA_BF16 the products
- * q.K and p.V run on bf16 tensor-core MMAs, p entering as the sum of two bf16
- * parts (about 16 significant bits); for PA_F32 on fp32 FMAs.  Results are deterministic for a given input and partition size.
+ * `workspace`.  With a workspace, the bf16 pass also hands out its work items
+ * through a counter held there, so CTAs that finish early take more.
+ * Arithmetic: fp32 accumulation; for PA_BF16 the products q.K and p.V run on
+ * bf16 tensor-core MMAs, p entering as the sum of two bf16 parts (about 16
+ * significant bits); for PA_F32 on fp32 FMAs.  Results are deterministic for
+ * a given input and partition size (which CTA runs an item does not change
+ * its arithmetic).
  */
 typedef struct pa_decode_args {
     int num_seqs;           /* S >= 0 */
@@ -98,8 +102,12 @@ typedef struct pa_decode_args {
                                [16, 4096]; 0 picks 512 */
     int max_context_len;    /* host upper bound of context_lens[i]; longer
                                entries are clamped and flagged */
-    void *workspace;        /* device scratch for split-K partials; may be NULL
-                               when max_context_len <= partition_size */
+    void *workspace;        /* device scratch, 256-byte aligned is best: the
+                               partition pass's work counter in its first 8
+                               bytes, then the split-K partials; may be NULL
+                               when max_context_len <= partition_size.  No
+                               part needs to start at zero (see
+                               skip_counter_reset). */
     size_t workspace_bytes; /* >= pa_decode_workspace_size(...) */
     int32_t *dev_status;    /* optional device word for PA_STATUS_* bits */
     void *stream;           /* cudaStream_t */
@@ -128,6 +136,16 @@ typedef struct pa_decode_args {
                                0, the default, uses the MMAs.  Same results
                                within the tolerance; for comparison and for
                                callers who want fp32 products throughout. */
+    int skip_counter_reset; /* The bf16 pass hands out work items through a
+                               counter at the start of the workspace.  Each
+                               call leaves that counter zero when it completes,
+                               and by default also zeroes it first with a
+                               cudaMemsetAsync on `stream` (8 bytes).  Nonzero
+                               skips that memset (one operation, a few
+                               microseconds, fewer per call): valid once the
+                               counter is zero, i.e. after any completed call
+                               on this workspace, or when the caller zeroed its
+                               first 8 bytes. */
 } pa_decode_args;
 
 #define PA_PHASE_ALL 0
@@ -165,7 +183,9 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  *    call before any stream capture on the device.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents; no part of it needs to start at zero (each call writes every
- *    partial it reads).  Calls that overlap on the GPU -- on different streams
+ *    partial it reads, and the work counter is reset before each pass unless
+ *    skip_counter_reset is set; the array starts at zero and each completed
+ *    call leaves the counter zero, so setting it is valid here).  Calls that overlap on the GPU -- on different streams
  *    without ordering between them -- race on the array. */
 #define PA_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 

@@ -61,6 +61,7 @@ class _DecodeArgs(ctypes.Structure):
         ("v_new", ctypes.c_void_p),
         ("slot_mapping", ctypes.c_void_p),
         ("simt", ctypes.c_int),
+        ("skip_counter_reset", ctypes.c_int),
     ]
 
 
@@ -203,14 +204,17 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
               max_context_len: int, partition_size: int = 0, workspace: torch.Tensor | None = None,
               status: DeviceStatus | None = None, stream=None, phase: int = 0,
               k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
-              slot_mapping: torch.Tensor | None = None, simt: bool = False) -> torch.Tensor:
+              slot_mapping: torch.Tensor | None = None, simt: bool = False,
+              skip_counter_reset: bool = False) -> torch.Tensor:
     """Paged decode attention; writes ``out`` [S, Hq, hd] and returns it.
 
     q [S, Hq, hd]; k_cache, v_cache [num_blocks, Hkv, block_size, hd];
     block_tables [S, max_blocks] int32; context_lens [S] int32.  When any
     sequence may span more than one partition a workspace of
     ``pa_decode_workspace_size`` bytes is needed; if none is given one is
-    allocated with torch for this call.
+    allocated (zeroed) with torch for this call.  ``skip_counter_reset=True``
+    skips the reset of the workspace's work counter; valid when the counter is
+    zero (a zeroed workspace, or one a completed call has used).
 
     With k_new, v_new [S, Hkv, hd] and slot_mapping [S] int64, each
     sequence's new (last) token is written into the caches and attended in the
@@ -234,7 +238,8 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
         raise ValueError("inconsistent shapes")
     need = pa_decode_workspace_size(S, Hq, hd, max_context_len, partition_size)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+        skip_counter_reset = True
     if workspace is not None:
         _check_cuda(workspace, "workspace", (torch.uint8,), dev)
     fused = (k_new, v_new, slot_mapping)
@@ -256,7 +261,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
                        k_new.data_ptr() if k_new is not None else None,
                        v_new.data_ptr() if v_new is not None else None,
                        slot_mapping.data_ptr() if slot_mapping is not None else None,
-                       1 if simt else 0)
+                       1 if simt else 0, 1 if skip_counter_reset else 0)
     with torch.cuda.device(dev):
         rc = _lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                             block_tables.data_ptr(), context_lens.data_ptr(), Hq, Hkv, hd, bs,

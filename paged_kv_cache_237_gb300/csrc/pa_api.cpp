@@ -18,4 +18,4 @@ int pa_fail(int code, const char *msg) {
 
 extern "C" const char *pa_last_error_string(void) { return g_last_error.c_str(); }
 
-extern "C" int pa_version(void) { return (1 << 16) | 0; }
+extern "C" int pa_version(void) { return (1 << 16) | 1; }

@@ -10,8 +10,10 @@
 // HBM bandwidth ("PagedAttention", robocikowo.com, "Zlozonosc obliczeniowa").
 //
 // Work decomposition.  A work item is (sequence, context partition, KV head,
-// query-head tile).  A persistent grid walks the items in order; a CTA owns an
-// item and its 4 warps split the item's 16-token chunks round-robin.  Each warp
+// query-head tile).  A persistent grid walks the items in order, each CTA
+// taking the next unclaimed item from a device counter (bf16 path with a
+// workspace); a CTA owns an item and its 4 warps split the item's 16-token
+// chunks round-robin.  Each warp
 // runs its own ring of NSTAGE shared-memory stages, filled by TMA and tracked
 // by one mbarrier per stage, so the main loop needs no CTA-wide barrier.  At
 // the end of the item the warps' partial softmax states (max, sum, unnormalised
@@ -221,6 +223,19 @@ __device__ __forceinline__ NewToken new_token(const DecodeParams &p, const Item 
     return t;
 }
 
+// Work counter of the partition pass (one 64-bit word): hand-outs in the low
+// half, finished CTAs in the high half.  Every CTA makes all its hand-out
+// requests before it reports finishing, so when the last CTA reports, no
+// request is left and the word can go back to zero for the next launch.
+__device__ __forceinline__ long long next_handout(unsigned long long *ctr) {
+    return static_cast<long long>(atomicAdd(ctr, 1ull) & 0xffffffffull);
+}
+
+__device__ __forceinline__ void finish_handouts(unsigned long long *ctr) {
+    const unsigned long long before = atomicAdd(ctr, 1ull << 32);
+    if ((before >> 32) == gridDim.x - 1u) atomicExch(ctr, 0ull);
+}
+
 // ------------------------------------------------------------ bf16 path ---
 template <int HD, int NSTAGE, bool ROWS16>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -258,7 +273,21 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int oob_row = p.total_rows;
     const uint64_t kv_policy = l2_evict_first_policy();
 
-    for (long long item = blockIdx.x;; item += gridDim.x) {
+    // Work items: a CTA's first is blockIdx.x; later ones come from the work
+    // counter in the workspace when there is one (a CTA that finishes early
+    // takes more), else every gridDim.x-th.  Either way a CTA's items increase,
+    // as the forward-only sequence cursor needs.  Thread 0 fetches the next
+    // index one item ahead, so the atomic's latency hides behind the item.
+    // s_next is double-buffered: the main loop has no CTA-wide barrier between
+    // a warp's read of one entry and thread 0's next write to it.  The
+    // counter's low 32 bits count hand-outs, its high 32 bits CTAs that have
+    // finished; the last CTA to finish sets it back to zero.
+    __shared__ long long s_next[2];
+    const bool dynamic = p.work_ctr != nullptr;
+    long long ahead = 0;
+    if (dynamic && threadIdx.x == 0) ahead = gridDim.x + next_handout(p.work_ctr);
+    int nb = 0;
+    for (long long item = blockIdx.x;;) {
         Item it;
         if (!next_item(it, cur, item, p, 16, lane)) break;
         const int my_n = it.nchunks > warp ? (it.nchunks - warp + kWarps - 1) / kWarps : 0;
@@ -490,12 +519,17 @@ __global__ void __launch_bounds__(kWarps * 32)
                 eo[16 * LD + 16 + g + 8] = ROWS16 ? l_hi : 0.f;
             }
         }
+        if (threadIdx.x == 0) s_next[nb] = dynamic ? ahead : item + gridDim.x;
         __syncthreads();
         merge_and_store<__nv_bfloat16, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows,
                                            it.single);
         fence_proxy_async_smem();
         __syncthreads();
+        item = s_next[nb];
+        nb ^= 1;
+        if (dynamic && threadIdx.x == 0) ahead = gridDim.x + next_handout(p.work_ctr);
     }
+    if (dynamic && threadIdx.x == 0) finish_handouts(p.work_ctr);
 
     // A wait gave up: let copies still in flight land before the CTA exits.
     if (failed && lane == 0) {
@@ -893,6 +927,11 @@ inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace layout: [work counter, 8 bytes, padded to 256] [partial (max, sum)]
+// [partial accumulators].  The counter sits at offset 0 whatever the sizes, so
+// a workspace reused for other sizes keeps a valid (zero) counter.
+constexpr size_t kWorkspaceHeader = 256;
+
 int effective_partition(int partition_size) { return partition_size == 0 ? 512 : partition_size; }
 
 }  // namespace
@@ -904,7 +943,7 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int he
     const long long max_parts = (max_context_len + P - 1) / P;
     if (max_parts <= 1) return 0;
     const size_t rows = static_cast<size_t>(num_seqs) * max_parts * num_q_heads;
-    return align256(rows * 2 * sizeof(float)) + rows * head_dim * sizeof(float);
+    return kWorkspaceHeader + align256(rows * 2 * sizeof(float)) + align256(rows * head_dim * sizeof(float));
 }
 
 extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -947,8 +986,10 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
         if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace))
             return pa_fail(PA_ERR_WORKSPACE, "pa_decode: workspace missing, unaligned or smaller than pa_decode_workspace_size()");
         const size_t rows = static_cast<size_t>(a->num_seqs) * max_parts * num_q_heads;
-        p.part_ml = static_cast<float *>(a->workspace);
-        p.part_acc = reinterpret_cast<float *>(static_cast<char *>(a->workspace) + align256(rows * 2 * sizeof(float)));
+        char *ws = static_cast<char *>(a->workspace);
+        p.work_ctr = reinterpret_cast<unsigned long long *>(ws);
+        p.part_ml = reinterpret_cast<float *>(ws + kWorkspaceHeader);
+        p.part_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader + align256(rows * 2 * sizeof(float)));
     }
     p.out = out;
     p.q = q;
@@ -990,6 +1031,9 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
         // only the merge pass below
     } else if (use_mma) {
         const bool rows16 = p.group > 8;
+        if (p.work_ctr && !a->skip_counter_reset &&
+            cudaMemsetAsync(p.work_ctr, 0, sizeof(unsigned long long), st) != cudaSuccess)
+            return pa_fail(PA_ERR_CUDA, "pa_decode: cannot reset the work counter");
         if (head_dim == 128)
             rc = rows16 ? launch_bf16<128, true>(p, k_cache, v_cache, items, dev, st)
                         : launch_bf16<128, false>(p, k_cache, v_cache, items, dev, st);
@@ -997,6 +1041,7 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
             rc = rows16 ? launch_bf16<64, true>(p, k_cache, v_cache, items, dev, st)
                         : launch_bf16<64, false>(p, k_cache, v_cache, items, dev, st);
     } else {
+        p.work_ctr = nullptr;   // the SIMT kernel walks its items statically
         if (a->dtype == PA_BF16)
             rc = head_dim == 128 ? launch_simt<__nv_bfloat16, 128>(p, items, dev, st)
                                  : launch_simt<__nv_bfloat16, 64>(p, items, dev, st);

@@ -31,6 +31,7 @@ struct DecodeParams {
     float *part_ml;        // [S][max_parts][Hq][2]  (running max in log2 units, sum)
     float *part_acc;       // [S][max_parts][Hq][HD] (unnormalised)
     int32_t *status;
+    unsigned long long *work_ctr;   // work items handed out so far (zeroed before each launch), or nullptr
     const void *k_new;     // fused cache write: [S][Hkv][HD] or nullptr
     const void *v_new;
     const int64_t *slot_mapping;

@@ -18,11 +18,17 @@ from .workloads import WORKLOADS, prefix_share_layout, randn
 
 class DecodeStep:
     """Holds the device buffers a repeated decode step needs (output,
-    split-K workspace, status word) so that the timed calls allocate nothing."""
+    split-K workspace, status word) so that the timed calls allocate nothing.
+
+    The workspace is zeroed once here, so the calls skip the per-call reset of
+    its work counter (every completed call leaves the counter zero).  Steps
+    that run one after another on one stream may share a workspace and a
+    status word: pass them in."""
 
     def __init__(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
-                 max_context_len: int, partition_size: int = 0, simt: bool = False):
+                 max_context_len: int, partition_size: int = 0, simt: bool = False,
+                 workspace: torch.Tensor | None = None, status: binding.DeviceStatus | None = None):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.scale = scale
@@ -32,8 +38,12 @@ class DecodeStep:
         self.out = torch.empty_like(q)
         S, Hq, hd = q.shape
         ws = binding.pa_decode_workspace_size(S, Hq, hd, max_context_len, partition_size)
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=q.device) if ws else None
-        self.status = binding.DeviceStatus(q.device)
+        if workspace is not None and workspace.numel() < ws:
+            raise ValueError(f"workspace has {workspace.numel()} bytes, {ws} needed")
+        if workspace is None and ws:
+            workspace = torch.zeros(ws, dtype=torch.uint8, device=q.device)
+        self.workspace = workspace if ws else None
+        self.status = status if status is not None else binding.DeviceStatus(q.device)
 
     def decode(self, stream=None, phase: int = binding.PA_PHASE_ALL, k_new=None, v_new=None,
                slot_mapping=None) -> torch.Tensor:
@@ -41,7 +51,8 @@ class DecodeStep:
                                  self.context_lens, self.scale, max_context_len=self.max_context_len,
                                  partition_size=self.partition_size, workspace=self.workspace,
                                  status=self.status, stream=stream, phase=phase, k_new=k_new,
-                                 v_new=v_new, slot_mapping=slot_mapping, simt=self.simt)
+                                 v_new=v_new, slot_mapping=slot_mapping, simt=self.simt,
+                                 skip_counter_reset=True)
 
     def run_fused(self, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                   cow_pairs: torch.Tensor | None = None, stream=None,

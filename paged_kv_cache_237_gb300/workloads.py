@@ -17,8 +17,9 @@ Workloads (sizes fixed here; the pages name the shapes only loosely):
     lengths uniform in [128, 2048], pool of ceil(1.2 x need) blocks, shuffled.
 ``gqa_llama3_70b``
     bf16, 32 sequences, 64 query / 8 KV heads, head_dim 128, block_size 16,
-    lengths round(4096 * exp(Z)), Z ~ N(0, 1), clipped to [256, 32768]; pool of
-    ceil(1.05 x need) blocks, shuffled.
+    lengths round(4096 * exp(sigma Z)), Z ~ N(0, 1), sigma 1 (0.5 as a
+    sensitivity case), clipped to [256, 32768]; pool of ceil(1.05 x need)
+    blocks, shuffled.
 ``prefix_share``
     bf16, 50 sequences, 32 query / 8 KV heads, head_dim 128, block_size 16: 25
     sampled pairs share one 2048-token prefix; each pair also shares a suffix
@@ -72,15 +73,18 @@ WORKLOADS = {
 }
 
 
-def context_lengths(w: Workload, rng: np.random.Generator) -> np.ndarray:
-    """Context length per sequence (int64), drawn per the workload's recipe."""
+def context_lengths(w: Workload, rng: np.random.Generator, gqa_sigma: float = 1.0) -> np.ndarray:
+    """Context length per sequence (int64), drawn per the workload's recipe.
+    ``gqa_sigma`` is the log-space spread of the GQA batch's lognormal (the
+    recipe leaves it open: 1.0 by default, 0.5 as a sensitivity case; the
+    same normal draws are scaled, so both cases share one median)."""
     if w.name == "tiny_f32":
         return np.array([7, 16, 33, 50], dtype=np.int64)
     if w.name == "mha_llama2_7b":
         return rng.integers(128, 2048, size=w.num_seqs, endpoint=True).astype(np.int64)
     if w.name == "gqa_llama3_70b":
         z = rng.standard_normal(w.num_seqs)
-        return np.clip(np.rint(4096.0 * np.exp(z)), 256, 32768).astype(np.int64)
+        return np.clip(np.rint(4096.0 * np.exp(gqa_sigma * z)), 256, 32768).astype(np.int64)
     if w.name == "long_context":
         short = rng.integers(16, 32768, size=w.num_seqs - 8, endpoint=True)
         lens = np.concatenate([np.full(8, 131072), short]).astype(np.int64)
@@ -146,7 +150,7 @@ def new_token_slots(lens: np.ndarray, tables: np.ndarray, block_size: int) -> np
 
 
 def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: bool = True,
-                  lens_override=None, block_size: int | None = None) -> dict:
+                  lens_override=None, block_size: int | None = None, gqa_sigma: float = 1.0) -> dict:
     """All inputs of one decode step of a workload (except prefix_share).
 
     Returns a dict with q [S, Hq, hd], k_cache/v_cache [num_blocks, Hkv, bs, hd],
@@ -155,7 +159,7 @@ def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: boo
     workload record and host copies of lengths and tables.  ``shuffle=False``
     places every sequence's blocks consecutively (identity placement);
     ``block_size`` overrides the workload's block size (same lengths, same
-    pool fill).
+    pool fill); ``gqa_sigma`` sets the GQA batch's lognormal spread.
     """
     w = WORKLOADS[name]
     if block_size is not None and block_size != w.block_size:
@@ -163,7 +167,7 @@ def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: boo
                      w.partition_size, w.seed, w.notes, w.extra)
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed)
-    lens = context_lengths(w, rng) if lens_override is None else np.asarray(lens_override, np.int64)
+    lens = context_lengths(w, rng, gqa_sigma) if lens_override is None else np.asarray(lens_override, np.int64)
     need = sum((int(n) + w.block_size - 1) // w.block_size for n in lens)
     nb = pool_blocks(w, need)
     tables, _ = place_blocks(lens, w.block_size, nb, rng, shuffle=shuffle)

@@ -66,11 +66,12 @@ def test_empty_batch_is_a_no_op(lib):
 def test_workspace_size_formula(lib):
     # no split needed
     assert lib.pa_decode_workspace_size(4, 8, 128, 512, 512) == 0
-    # 3 partitions of 512 for 1025 tokens: ml = 4*3*8*2 floats, acc = 4*3*8*128 floats
+    # 3 partitions of 512 for 1025 tokens: a 256-byte header (the work counter),
+    # then ml = 4*3*8*2 floats and acc = 4*3*8*128 floats, each padded to 256 bytes
     rows = 4 * 3 * 8
-    ml = rows * 8
-    ml_aligned = (ml + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(4, 8, 128, 1025, 512) == ml_aligned + rows * 128 * 4
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(4, 8, 128, 1025, 512) == 256 + a256(rows * 8) + a256(rows * 128 * 4)
+    assert lib.pa_decode_workspace_size(3, 5, 64, 1025, 512) == 256 + a256(45 * 8) + a256(45 * 64 * 4)
     assert lib.pa_decode_workspace_size(4, 8, 128, 1025, 0) == lib.pa_decode_workspace_size(4, 8, 128, 1025, 512)
 
 

@@ -276,3 +276,76 @@ def test_concurrent_first_calls_from_host_threads(pa):
     for i, (q, kc, vc, tables, lens_t) in enumerate(cases):
         ref = oracle_decode(q, kc, vc, tables, lens_t, 0.1)
         assert_decode_close(outs[i], ref, torch.bfloat16, what=f"thread {i}")
+
+
+def test_workspace_contents_do_not_matter(pa):
+    """The workspace may hold anything before a call: every partial is written
+    before it is read, and the work counter of the partition pass is reset on
+    the stream before the pass.  A workspace filled with 0xff bytes (NaN
+    partials, a huge counter) gives the same bits as a zeroed one, and both
+    match the oracle; so do later calls on it, with or without the reset.
+    Every call leaves the counter (the workspace's first 8 bytes) at zero."""
+    lens = [5000, 17, 2049, 4096, 600, 1]
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=21)
+    max_ctx = int(lens_t.max().item())
+    need = pa.pa_decode_workspace_size(len(lens), 16, 128, max_ctx, 256)
+    assert need > 0
+    zeroed = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    dirty = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    # the third call finds the second's contents; the fourth also skips the
+    # counter reset, valid because every completed call leaves the counter zero
+    for ws, skip in ((zeroed, False), (dirty, False), (dirty, False), (dirty, True)):
+        out = torch.empty_like(q)
+        status = pa.DeviceStatus()
+        pa.pa_decode(out, q, kc, vc, tables, lens_t, 0.09, max_context_len=max_ctx, partition_size=256,
+                     workspace=ws, status=status, skip_counter_reset=skip)
+        torch.cuda.synchronize()
+        assert status.read() == 0
+        assert int(ws[:8].view(torch.int64).item()) == 0, "the work counter must be left at zero"
+        outs.append(out)
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 0.09)
+    assert_decode_close(outs[0], ref, torch.bfloat16, what="zeroed workspace")
+    for out in outs[1:]:
+        assert torch.equal(out.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_work_counter_survives_phases_graphs_and_size_changes(pa):
+    """The self-resetting work counter across the ways a workspace is reused:
+    split phases, CUDA-graph replays, and calls of other sizes on the same
+    buffer, all with the reset skipped after the first call."""
+    lens = [3000, 700, 4096, 1, 513]
+    q, kc, vc, tables, lens_t = make_case(lens, 8, 1, 128, 32, torch.bfloat16, seed=33)
+    max_ctx = int(lens_t.max().item())
+    ws = torch.zeros(pa.pa_decode_workspace_size(64, 64, 128, 8192, 128), dtype=torch.uint8, device="cuda")
+    status = pa.DeviceStatus()
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 0.1)
+
+    def call(out, phase=0, P=128, **kw):
+        pa.pa_decode(out, q, kc, vc, tables, lens_t, 0.1, max_context_len=max_ctx, partition_size=P,
+                     workspace=ws, status=status, phase=phase, skip_counter_reset=True, **kw)
+
+    a = torch.empty_like(q)
+    call(a)
+    b = torch.empty_like(q)
+    call(b, phase=pa.PA_PHASE_PARTITIONS)
+    call(b, phase=pa.PA_PHASE_REDUCE)
+    torch.cuda.synchronize()
+    assert status.read() == 0 and int(ws[:8].view(torch.int64).item()) == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert_decode_close(a, ref, torch.bfloat16, what="skip reset")
+    c = torch.empty_like(q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(c)
+    for _ in range(3):
+        c.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c.view(torch.int16), a.view(torch.int16))
+    for P in (512, 16, 128):                       # other layouts of the partials, same counter word
+        d = torch.empty_like(q)
+        call(d, P=P)
+        torch.cuda.synchronize()
+        assert status.read() == 0 and int(ws[:8].view(torch.int64).item()) == 0
+        assert_decode_close(d, ref, torch.bfloat16, what=f"P={P} after other sizes")

@@ -22,9 +22,9 @@ def bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
 
 
-def step_and_check(pa, name, full=True):
+def step_and_check(pa, name, full=True, **kw):
     binding, engine, workloads = pa
-    d = workloads.decode_inputs(name, device="cuda")
+    d = workloads.decode_inputs(name, device="cuda", **kw)
     w = d["workload"]
     step = engine.DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                              d["scale"], d["max_context_len"], w.partition_size)
@@ -46,9 +46,10 @@ def test_tiny_f32_step(pa):
     assert_decode_close(out, ref, torch.float32, what="tiny_f32")
 
 
-@pytest.mark.parametrize("name", ["mha_llama2_7b", "gqa_llama3_70b"])
-def test_bf16_workload_step_full_parity(pa, name):
-    d, step, out, kc0, vc0 = step_and_check(pa, name)
+@pytest.mark.parametrize("name,kw", [("mha_llama2_7b", {}), ("gqa_llama3_70b", {}),
+                                     ("gqa_llama3_70b", {"gqa_sigma": 0.5})])
+def test_bf16_workload_step_full_parity(pa, name, kw):
+    d, step, out, kc0, vc0 = step_and_check(pa, name, **kw)
     oracle.reshape_and_cache(d["k_new"].cpu(), d["v_new"].cpu(), kc0, vc0, d["slot_mapping"].cpu())
     assert torch.equal(bits(d["k_cache"].cpu()), bits(kc0))
     ref = oracle_decode(d["q"], kc0, vc0, d["block_tables"], d["context_lens"], d["scale"])

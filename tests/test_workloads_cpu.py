@@ -1,0 +1,68 @@
+"""The seeded input recipes: lengths, placement and cache-write slots of the
+synthetic workloads, checked on the host (no cache values are drawn)."""
+import math
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_237_gb300.workloads import (WORKLOADS, context_lengths, new_token_slots, place_blocks,
+                                                pool_blocks)
+
+
+def lengths(name, **kw):
+    w = WORKLOADS[name]
+    return w, context_lengths(w, np.random.default_rng(w.seed), **kw)
+
+
+def test_length_recipes():
+    _, n = lengths("tiny_f32")
+    assert n.tolist() == [7, 16, 33, 50]
+    w, n = lengths("mha_llama2_7b")
+    assert len(n) == w.num_seqs == 64 and n.min() >= 128 and n.max() <= 2048
+    w, n = lengths("long_context")
+    assert len(n) == 256 and int((n == 131072).sum()) == 8
+    rest = n[n != 131072]
+    assert rest.min() >= 16 and rest.max() <= 32768
+    assert int(n.sum()) == 5_074_911                    # the figure the benchmark reports
+
+
+def test_gqa_lognormal_and_its_sensitivity_case():
+    w, a = lengths("gqa_llama3_70b")
+    _, b = lengths("gqa_llama3_70b", gqa_sigma=0.5)
+    assert len(a) == len(b) == 32
+    assert a.min() >= 256 and a.max() <= 32768 and b.min() >= 256 and b.max() <= 32768
+    # same normal draws, scaled: where neither is clipped, log(n / 4096) halves
+    z = np.random.default_rng(w.seed).standard_normal(32)
+    free = (np.abs(z) < math.log(8)) & (a > 256) & (a < 32768)
+    assert np.allclose(np.log(b[free] / 4096.0), 0.5 * np.log(a[free] / 4096.0), atol=2e-3)
+    assert np.std(np.log(b)) < np.std(np.log(a))
+    assert int(a.sum()) == 219_876
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "long_context"])
+def test_placement_is_a_valid_paging(name):
+    w, n = lengths(name)
+    per = [-(-int(x) // w.block_size) for x in n]
+    nb = pool_blocks(w, sum(per))
+    tables, need = place_blocks(n, w.block_size, nb, np.random.default_rng(1))
+    assert need == sum(per) <= nb
+    used = []
+    for i, k in enumerate(per):
+        row = tables[i]
+        assert (row[:k] >= 0).all() and (row[:k] < nb).all() and (row[k:] == -1).all()
+        used.extend(row[:k].tolist())
+    assert len(set(used)) == len(used)                  # no block is shared: private pages
+    if name == "long_context":
+        assert 0.955 <= need / nb <= 0.961
+    ident, _ = place_blocks(n, w.block_size, nb, np.random.default_rng(1), shuffle=False)
+    assert ident[0, :per[0]].tolist() == list(range(per[0]))
+
+
+def test_new_token_slot_is_the_last_position():
+    w, n = lengths("gqa_llama3_70b")
+    per = [-(-int(x) // w.block_size) for x in n]
+    tables, _ = place_blocks(n, w.block_size, pool_blocks(w, sum(per)), np.random.default_rng(2))
+    slots = new_token_slots(n, tables, w.block_size)
+    for i, x in enumerate(n):
+        blk, off = divmod(int(slots[i]), w.block_size)
+        assert blk == tables[i, (int(x) - 1) // w.block_size] and off == (int(x) - 1) % w.block_size
