@@ -44,31 +44,35 @@ L2_BYTES = 129 * 2**20
 # full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
 # source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "1fa091a52640c95c",
-                   "bytes_per_launch": {"long_context": 20802785280 + 295916800,
-                                        "gqa_llama3_70b": 902333184 + 6208512}}
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "4082a100ebdbdaf3",
+                   "bytes_per_launch": {"long_context": 20801963008 + 298790912,
+                                        "gqa_llama3_70b": 902333696 + 6109184}}
 
 
-def kernel_source(text: bytes) -> bytes:
-    """The code the bf16 partition pass is compiled from: pa_decode.cu up to
-    the SIMT kernel (includes, device helpers, the bf16 kernel), with comments
-    and whitespace removed so that only code changes count."""
+def kernel_source(*texts: bytes) -> bytes:
+    """The code the bf16 partition pass is built and launched from (pa_decode.cu
+    and pa_internal.h: kernels, helpers, launch shapes), with comments and
+    whitespace removed so that only code changes count."""
     import re
-    cut = text.find(b"// ------------------------------------------------------------ SIMT path ---")
-    code = text if cut < 0 else text[:cut]
-    code = re.sub(rb"/\*.*?\*/", b"", code, flags=re.S)
-    code = re.sub(rb"//[^\n]*", b"", code)
-    return re.sub(rb"\s+", b" ", code).strip()
+    out = []
+    for text in texts:
+        code = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+        code = re.sub(rb"//[^\n]*", b"", code)
+        out.append(re.sub(rb"\s+", b" ", code).strip())
+    return b"\n".join(out)
 
 
 def captured_traffic(workload: str):
     """Measured DRAM bytes of one partition-pass launch of `workload`, or None
     when there is no capture of it or the kernel changed since."""
     import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc", "pa_decode.cu")
+    csrc = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc")
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(kernel_source(f.read())).hexdigest()[:16]
+        texts = []
+        for name in ("pa_decode.cu", "pa_internal.h"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                texts.append(f.read())
+        digest = hashlib.sha256(kernel_source(*texts)).hexdigest()[:16]
     except OSError:
         return None
     c = TRAFFIC_CAPTURE

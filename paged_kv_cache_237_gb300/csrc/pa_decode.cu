@@ -880,7 +880,11 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
 }
 
 template <int HD>
-constexpr int bf16_stages() { return HD == 128 ? 3 : 4; }
+// Ring depth per warp.  hd128: 2 stages of 8 KB (64 KB per CTA), so 3 CTAs fit
+// per SM (by shared memory and by 168 registers x 128 threads); with the
+// dynamic item hand-out this beats 3 stages at 2 CTAs per SM on every batch
+// measured.  hd64: 4 stages of 4 KB, also 3 CTAs per SM.
+constexpr int bf16_stages() { return HD == 128 ? 2 : 4; }
 template <typename T>
 constexpr int simt_stages() { return sizeof(T) == 4 ? 2 : 3; }
 
