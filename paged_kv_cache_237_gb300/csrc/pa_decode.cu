@@ -1030,6 +1030,9 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     if (sm_count(dev) <= 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot query the SM count");
     cudaStream_t st = static_cast<cudaStream_t>(a->stream);
     const long long items = static_cast<long long>(a->num_seqs) * max_parts * num_kv_heads * p.head_tiles;
+    // The work counter holds hand-out indices in 32 bits; beyond that (never
+    // reached by a cache that fits in memory) the fixed stride is used.
+    if (items >= (1ll << 31)) p.work_ctr = nullptr;
 
     int rc = PA_OK;
     if (a->phase == PA_PHASE_REDUCE) {

@@ -80,3 +80,27 @@ def test_noalloc_rejects_sizes_beyond_its_fixed_scratch(pa):
     assert b"PA_NOALLOC_WORKSPACE_BYTES" in pa._lib.pa_last_error_string()
     assert torch.count_nonzero(out) == 0       # nothing was enqueued
     del lens
+
+
+def test_noalloc_may_skip_the_counter_reset(pa):
+    """The fixed scratch starts at zero and every completed call leaves its
+    work counter at zero, so a caller may set skip_counter_reset: the same
+    bits come out as with the reset, call after call."""
+    lens = [3000, 700, 4096, 1, 513, 2049]
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=77)
+    max_ctx, P, scale = max(lens), 256, 0.09
+    outs = []
+    for skip in (0, 1, 1, 0, 1):
+        out = torch.full_like(q, float("nan"))
+        status = pa.DeviceStatus()
+        args = c_args(pa, q, kc, tables, max_ctx, P, status)
+        args.skip_counter_reset = skip
+        rc = pa._lib.pa_decode_noalloc(out.data_ptr(), q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                                       tables.data_ptr(), lens_t.data_ptr(), q.shape[1], kc.shape[1], q.shape[2],
+                                       kc.shape[2], ctypes.c_float(scale), ctypes.byref(args))
+        assert rc == 0, pa._lib.pa_last_error_string()
+        torch.cuda.synchronize()
+        assert status.read() == 0
+        outs.append(out)
+    for out in outs[1:]:
+        assert torch.equal(out.view(torch.int16), outs[0].view(torch.int16))
