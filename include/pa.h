@@ -66,7 +66,8 @@ extern "C" {
 /* ---- device status bits (OR-ed into *dev_status by the kernels) -------- */
 #define PA_STATUS_BAD_BLOCK_ID 1    /* block table entry outside [0, num_blocks) */
 #define PA_STATUS_BAD_CONTEXT_LEN 2 /* context_lens[i] < 0 or beyond the table or max_context_len */
-#define PA_STATUS_BAD_SLOT 4        /* slot_mapping entry >= num_blocks * block_size */
+#define PA_STATUS_BAD_SLOT 4        /* slot_mapping entry >= num_blocks * block_size, or (fused
+                                       write) not the slot of the sequence's last position */
 #define PA_STATUS_BAD_PAIR 8        /* copy pair out of range, or its dst is another pair's src/dst */
 #define PA_STATUS_WAIT_TIMEOUT 16   /* a bounded wait for staged data gave up */
 
@@ -185,8 +186,9 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  *    contents; no part of it needs to start at zero (each call writes every
  *    partial it reads, and the work counter is reset before each pass unless
  *    skip_counter_reset is set; the array starts at zero and each completed
- *    call leaves the counter zero, so setting it is valid here).  Calls that overlap on the GPU -- on different streams
- *    without ordering between them -- race on the array. */
+ *    call leaves the counter zero, so setting it is valid here).
+ *  - Calls that overlap on the GPU -- on different streams without ordering
+ *    between them -- race on the array. */
 #define PA_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 
 int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
