@@ -44,9 +44,9 @@ L2_BYTES = 129 * 2**20
 # full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
 # source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "13739f84c027e3ef",
-                   "bytes_per_launch": {"long_context": 20801801472 + 297060352,
-                                        "gqa_llama3_70b": 902394112 + 6099200}}
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "076b746c805e141e",
+                   "bytes_per_launch": {"long_context": 20801765120 + 298380544,
+                                        "gqa_llama3_70b": 902386944 + 5854464}}
 
 
 def kernel_source(*texts: bytes) -> bytes:

@@ -237,8 +237,20 @@ __device__ __forceinline__ void finish_handouts(unsigned long long *ctr) {
 }
 
 // ------------------------------------------------------------ bf16 path ---
+// Launch shape per head_dim: ring depth per warp and the CTAs per SM the
+// kernel is built for (its launch bounds hold registers to what that needs).
+// hd128: 2 stages of 8 KB (64 KB of stages per CTA), 3 CTAs per SM (shared
+// memory, and 168 registers x 128 threads x 3); with the dynamic item hand-out
+// this beats 3 stages at 2 CTAs per SM on every batch measured.  hd64: 3
+// stages of 4 KB (48 KB per CTA), 4 CTAs per SM, 3-6 % faster than 4 stages at
+// 3 CTAs per SM.
+template <int HD>
+constexpr int bf16_stages() { return HD == 128 ? 2 : 3; }
+template <int HD>
+constexpr int bf16_ctas_per_sm() { return HD == 128 ? 3 : 4; }
+
 template <int HD, int NSTAGE, bool ROWS16>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, bf16_ctas_per_sm<HD>())
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
     constexpr int HALVES = HD / 64;              // 128-byte column slices per row
@@ -879,20 +891,14 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
     return r == CUDA_SUCCESS;
 }
 
-template <int HD>
-// Ring depth per warp.  hd128: 2 stages of 8 KB (64 KB per CTA), so 3 CTAs fit
-// per SM (by shared memory and by 168 registers x 128 threads); with the
-// dynamic item hand-out this beats 3 stages at 2 CTAs per SM on every batch
-// measured.  hd64: 3 stages of 4 KB (48 KB per CTA), 4 CTAs per SM, which beats
-// 4 stages at 3 CTAs per SM by 3-6 %.
-constexpr int bf16_stages() { return HD == 128 ? 2 : 3; }
+
 template <typename T>
 constexpr int simt_stages() { return sizeof(T) == 4 ? 2 : 3; }
 
 template <int HD, bool ROWS16>
 int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache, long long items,
                 int dev, cudaStream_t st) {
-    constexpr int NS = bf16_stages<HD>();
+    constexpr int NS = pa::bf16_stages<HD>();
     constexpr int STAGE = 2 * (HD / 64) * pa::kChunk * 128;
     constexpr int SMEM = pa::kWarps * NS * STAGE + pa::kWarps * NS * 8 + 1024;
     static KernelSlot slot;
