@@ -297,12 +297,13 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="write the new tokens with a separate pa_reshape_and_cache launch instead of inside "
                          "the decode launch")
-    ap.add_argument("--study", choices=["placement", "prefix_cache", "swap", "mma"], default=None,
+    ap.add_argument("--study", choices=["placement", "prefix_cache", "swap", "mma", "cache_ops"], default=None,
                     help="instead of the benchmark line, print one study line: 'placement' times the partition "
                          "pass with shuffled vs identity block placement at block sizes 32 and 16; "
                          "'prefix_cache' admits a multi-tenant batch through the chained-key prefix cache and "
                          "times its decode step; 'swap' times block copies between the device cache and pinned "
-                         "host memory; 'mma' times the bf16 partition pass on tensor-core MMAs vs SIMT FMAs")
+                         "host memory; 'mma' times the bf16 partition pass on tensor-core MMAs vs SIMT FMAs; "
+                         "'cache_ops' times the cache write and the block copy at step and streaming sizes")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.study == "placement":
@@ -313,6 +314,9 @@ def main():
         return
     if args.study == "swap":
         run_swap_study(args)
+        return
+    if args.study == "cache_ops":
+        run_cache_ops_study(args)
         return
     if args.study == "mma":
         run_mma_study(args)
@@ -796,6 +800,76 @@ def run_swap_study(args, num_blocks: int = 4096):
                       "contiguous_memcpy_out_GBps": round(nbytes / (mc_out * 1e-3) / 1e9, 1),
                       "contiguous_memcpy_in_GBps": round(nbytes / (mc_in * 1e-3) / 1e9, 1)}),
           flush=True)
+
+
+def run_cache_ops_study(args):
+    """pa_reshape_and_cache and pa_copy_blocks at decode-step sizes (latency)
+    and at sizes where they stream HBM: the long-context geometry (8 KV heads,
+    block_size 32, head_dim 128, bf16), distinct random slots and pairs, CUDA
+    graphs of single launches, inputs larger than L2 where the size allows
+    (a 512 MB buffer is written between launches otherwise).  Bytes are read +
+    written bytes of the cache rows or blocks moved."""
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.workloads import randn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    Hkv, bs, hd = 8, 32, 128
+    pool = 40000                                  # 2.6 GB per cache
+    kc = randn((pool, Hkv, bs, hd), torch.bfloat16, 91, dev)
+    vc = randn((pool, Hkv, bs, hd), torch.bfloat16, 92, dev)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+    status = binding.DeviceStatus(dev)
+    stream = torch.cuda.current_stream()
+    rng = np.random.default_rng(13)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+
+    def timed(fn, flush_between):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):          # fn launches on the current (capturing) stream
+            fn()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            if flush_between:
+                flush_l2(flush)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    rows = {}
+    for T in (256, 4096, 65536):
+        k = randn((T, Hkv, hd), torch.bfloat16, 93, dev)
+        v = randn((T, Hkv, hd), torch.bfloat16, 94, dev)
+        slots = torch.from_numpy(rng.choice(pool * bs, size=T, replace=False).astype(np.int64)).to(dev)
+        nbytes = T * Hkv * hd * 2 * 2 * 2 + T * 8
+        ms = timed(lambda: binding.pa_reshape_and_cache(k, v, kc, vc, slots, status=status),
+                   nbytes < 2 * L2_BYTES)
+        rows[f"reshape_and_cache_T{T}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                           "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+    for P in (24, 256, 2048):
+        ids = rng.choice(pool, size=2 * P, replace=False)
+        pairs = torch.from_numpy(np.stack([ids[:P], ids[P:]], 1).astype(np.int64)).to(dev)
+        nbytes = P * 2 * Hkv * bs * hd * 2 * 2 + P * 16
+        ms = timed(lambda: binding.pa_copy_blocks(kc, vc, pairs, status=status),
+                   nbytes < 2 * L2_BYTES)
+        rows[f"copy_blocks_P{P}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+    if status.read():
+        raise RuntimeError("device status flagged an input error")
+    print(json.dumps({"study": "cache_ops", "geometry": "8 KV heads, block_size 32, head_dim 128, bf16",
+                      "peak_GBps": peak, "results": rows}), flush=True)
 
 
 def measure_step(name: str, steps: int, warmup: int = 5, gqa_sigma: float = 1.0) -> dict:

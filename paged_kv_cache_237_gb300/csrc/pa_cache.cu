@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128)
 }
 
 // grid (num_pairs, 2): blockIdx.y selects the K or the V cache.  Before
-// copying, the CTA checks its pair against every other pair: a dst that is
+// writing, the CTA checks its pair against every other pair: a dst that is
 // duplicated or that another pair reads is a race, so the pair is skipped and
 // flagged.
 __global__ void __launch_bounds__(256)
@@ -64,6 +64,20 @@ __global__ void __launch_bounds__(256)
         return;
     }
     if (src == dst) return;
+    uint4 *cache = blockIdx.y == 0 ? k_cache : v_cache;
+    const uint4 *from = cache + src * block_vecs;
+    uint4 *to = cache + dst * block_vecs;
+    // The first kPre vectors of the block are loaded before the conflict scan,
+    // so that the scan's round trip overlaps theirs.  Reading src early is
+    // safe: a pair whose dst is our src is itself flagged and skipped, so
+    // nothing writes src during this launch.
+    constexpr int kPre = 8;
+    uint4 pre[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const long long i = threadIdx.x + static_cast<long long>(u) * blockDim.x;
+        if (i < block_vecs) pre[u] = from[i];
+    }
     for (int j = threadIdx.x; j < num_pairs; j += blockDim.x) {
         if (j == pidx) continue;
         const int64_t s2 = pairs[2 * j], d2 = pairs[2 * j + 1];
@@ -74,10 +88,12 @@ __global__ void __launch_bounds__(256)
         if (threadIdx.x == 0 && blockIdx.y == 0) flag_status(status, PA_STATUS_BAD_PAIR);
         return;
     }
-    uint4 *cache = blockIdx.y == 0 ? k_cache : v_cache;
-    const uint4 *from = cache + src * block_vecs;
-    uint4 *to = cache + dst * block_vecs;
-    long long i = threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const long long i = threadIdx.x + static_cast<long long>(u) * blockDim.x;
+        if (i < block_vecs) to[i] = pre[u];
+    }
+    long long i = threadIdx.x + static_cast<long long>(kPre) * blockDim.x;
     // four independent 16-byte loads in flight per thread
     for (; i + 3 * blockDim.x < block_vecs; i += 4 * blockDim.x) {
         const uint4 a = from[i], b = from[i + blockDim.x], c = from[i + 2 * blockDim.x],
