@@ -756,7 +756,10 @@ template <typename OutT, int HD>
 __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qh = blockIdx.x;
-    const int seq = blockIdx.y;
+    // Newest partials first when they do not all fit in L2: the partition pass
+    // writes them in sequence order, so the last sequences' are still in L2.
+    const int seq = p.reduce_newest_first ? p.num_seqs - 1 - static_cast<int>(blockIdx.y)
+                                          : static_cast<int>(blockIdx.y);
     const int n = seq_len(p, seq);
     if (n <= p.partition_size) return;
     const int np = (n + p.partition_size - 1) / p.partition_size;
@@ -840,6 +843,19 @@ EncodeTiledFn encode_tiled() {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
+}
+
+long long l2_bytes(int dev) {
+    static std::atomic<long long> cache[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    long long b = cache[dev].load(std::memory_order_relaxed);
+    if (b == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+        b = v;
+        cache[dev].store(b, std::memory_order_relaxed);
+    }
+    return b;
 }
 
 int sm_count(int dev) {
@@ -1036,6 +1052,11 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     if (sm_count(dev) <= 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot query the SM count");
     cudaStream_t st = static_cast<cudaStream_t>(a->stream);
     const long long items = static_cast<long long>(a->num_seqs) * max_parts * num_kv_heads * p.head_tiles;
+    // Upper bound of the partial bytes a step writes; above the L2 size the
+    // merge reads the newest partials first, while they are still there.
+    const long long partial_bytes =
+        static_cast<long long>(a->num_seqs) * max_parts * num_q_heads * (head_dim + 2) * 4;
+    p.reduce_newest_first = max_parts > 1 && partial_bytes > l2_bytes(dev) ? 1 : 0;
     // The work counter holds hand-out indices in 32 bits; beyond that (never
     // reached by a cache that fits in memory) the fixed stride is used.
     if (items >= (1ll << 31)) p.work_ctr = nullptr;

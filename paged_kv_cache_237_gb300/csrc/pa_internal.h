@@ -41,6 +41,7 @@ struct DecodeParams {
     int block_size, num_blocks, max_blocks_per_seq;
     int partition_size, max_parts, ctx_cap;
     int total_rows;        // num_blocks * num_kv_heads * block_size (TMA row extent)
+    int reduce_newest_first;   // merge pass walks sequences last to first
     float scale_log2;      // scale * log2(e)
 };
 
