@@ -250,23 +250,32 @@ def time_oracle(d, seqs, threads):
 
 
 def pick_sample(d, target_s: float, threads: int):
-    """Sequences (seeded order, shortest first among a random draw) whose
-    oracle time is about target_s; returns (seqs, est_seconds)."""
+    """Sequences (seeded random order) whose oracle time is about target_s.
+    The rate per token comes from one probe sequence, then from one timed run
+    of the picked sample if that overshoots by more than a quarter."""
     lens = d["lens"]
     rng = np.random.default_rng(1234)
     order = [int(i) for i in rng.permutation(len(lens))]
+
+    def pick(per_token):
+        budget = target_s / per_token
+        seqs, tok = [], 0
+        for s in order:
+            if tok + int(lens[s]) > budget and seqs:
+                continue
+            seqs.append(s)
+            tok += int(lens[s])
+            if tok >= 0.9 * budget:
+                break
+        return seqs, tok
+
     probe = order[:1]
     dt = max(time_oracle(d, probe, threads), 1e-4)
-    per_token = dt / max(1, int(lens[probe[0]]))
-    budget = target_s / per_token
-    seqs, tok = [], 0
-    for s in order:
-        if tok + int(lens[s]) > budget and seqs:
-            continue
-        seqs.append(s)
-        tok += int(lens[s])
-        if tok >= 0.9 * budget:
-            break
+    seqs, tok = pick(dt / max(1, int(lens[probe[0]])))
+    if len(seqs) > 1:
+        dt = time_oracle(d, seqs, threads)
+        if dt > 1.25 * target_s:
+            seqs, _ = pick(dt / max(1, tok))
     return seqs
 
 
@@ -990,7 +999,7 @@ def run_reference(args):
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     d = workloads.decode_inputs(name, device=device, gqa_sigma=args.gqa_sigma)
     threads = host_cores()
-    per_step = max(0.5, min(10.0, 150.0 / (args.steps + args.warmup)))
+    per_step = max(0.3, min(10.0, 150.0 / (args.steps + args.warmup)))
     seqs = pick_sample(d, per_step, threads)
     sb = sample_kv_bytes(d, seqs)
     import oracle
