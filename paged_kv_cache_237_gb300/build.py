@@ -93,7 +93,7 @@ def _compile(verbose: bool, ptxas_verbose: bool) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"compile failed: {cmd[-3]}")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-lpthread"]
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-lpthread", "-ldl"]
     r = subprocess.run(link, capture_output=True, text=True)
     if verbose or r.returncode != 0:
         sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)

@@ -178,6 +178,7 @@ extern "C" int pa_reshape_and_cache(const void *k, const void *v, void *k_cache,
                                     const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                                     int head_dim, int block_size, int num_blocks, int dtype,
                                     int32_t *dev_status, void *stream) {
+    PaTraceRange trace("pa_reshape_and_cache");
     const int eb = elem_bytes(dtype);
     if (eb == 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: bad dtype");
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
@@ -203,6 +204,7 @@ extern "C" int pa_reshape_and_cache(const void *k, const void *v, void *k_cache,
 extern "C" int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs,
                               int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
                               int32_t *dev_status, void *stream) {
+    PaTraceRange trace("pa_copy_blocks");
     const int eb = elem_bytes(dtype);
     if (eb == 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: bad dtype");
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
@@ -227,6 +229,7 @@ extern "C" int pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k,
                               const int64_t *src_dst_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks,
                               int num_kv_heads, int head_dim, int block_size, int dtype, int32_t *dev_status,
                               void *stream) {
+    PaTraceRange trace("pa_swap_blocks");
     const int eb = elem_bytes(dtype);
     if (eb == 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: bad dtype");
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || src_num_blocks <= 0 ||

@@ -977,6 +977,7 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
                          const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
                          int num_kv_heads, int head_dim, int block_size, float scale,
                          const pa_decode_args *a) {
+    PaTraceRange trace("pa_decode");
     if (!a) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: args is NULL");
     if (a->num_seqs < 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs < 0");
     if (a->num_seqs == 0) return PA_OK;
@@ -1139,6 +1140,7 @@ extern "C" int pa_decode_noalloc(void *out, const void *q, const void *k_cache, 
                                  const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, float scale,
                                  const pa_decode_args *args) {
+    PaTraceRange trace("pa_decode_noalloc");
     if (!args) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode_noalloc: args is NULL");
     if (args->num_seqs == 0) return PA_OK;
     const int P = effective_partition(args->partition_size);

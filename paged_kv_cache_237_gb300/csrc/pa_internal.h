@@ -13,6 +13,18 @@ int pa_fail(int code, const char *msg);
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
+// Names the enclosing API call as an NVTX range, so profiler timelines show
+// which call enqueued which kernels.  Without a profiler attached the calls do
+// nothing.
+struct PaTraceRange {
+    explicit PaTraceRange(const char *name) { nvtxRangePushA(name); }
+    ~PaTraceRange() { nvtxRangePop(); }
+    PaTraceRange(const PaTraceRange &) = delete;
+    PaTraceRange &operator=(const PaTraceRange &) = delete;
+};
+
 namespace pa {
 
 constexpr int kWarps = 4;        // warps per decode CTA

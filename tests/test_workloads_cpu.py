@@ -66,3 +66,19 @@ def test_new_token_slot_is_the_last_position():
     for i, x in enumerate(n):
         blk, off = divmod(int(slots[i]), w.block_size)
         assert blk == tables[i, (int(x) - 1) // w.block_size] and off == (int(x) - 1) % w.block_size
+
+
+def test_generators_are_deterministic():
+    """Same seed, same inputs, bit for bit (both sides of every parity test
+    are fed from these generators); another seed gives other values."""
+    import torch
+    from paged_kv_cache_237_gb300.workloads import decode_inputs, randn
+    a, b = decode_inputs("tiny_f32"), decode_inputs("tiny_f32")
+    for key in ("q", "k_cache", "v_cache", "block_tables", "context_lens", "k_new", "v_new", "slot_mapping"):
+        assert torch.equal(a[key], b[key]), key
+    x = randn((3, 1000), torch.bfloat16, 5, "cpu")
+    assert torch.equal(x.view(torch.int16), randn((3, 1000), torch.bfloat16, 5, "cpu").view(torch.int16))
+    assert not torch.equal(x, randn((3, 1000), torch.bfloat16, 6, "cpu"))
+    # chunked drawing equals one draw of the same stream
+    assert torch.equal(randn((4, 100), torch.float32, 9, "cpu", chunk_elems=64),
+                       randn((4, 100), torch.float32, 9, "cpu"))
