@@ -44,9 +44,9 @@ L2_BYTES = 129 * 2**20
 # full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
 # (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
 # source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "4d36717889df5aa5",
-                   "bytes_per_launch": {"long_context": 20802539776 + 298108672,
-                                        "gqa_llama3_70b": 902333696 + 6054912}}
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "88d26b8f68a9cc31",
+                   "bytes_per_launch": {"long_context": 20801741824 + 297158144,
+                                        "gqa_llama3_70b": 902382592 + 6171648}}
 
 
 def kernel_source(*texts: bytes) -> bytes:

@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kWarps * 32, bf16_ctas_per_sm<HD>())
         nb ^= 1;
         if (dynamic && threadIdx.x == 0) ahead = gridDim.x + next_handout(p.work_ctr);
     }
+    // No more items for this CTA: the merge launch may start taking its place
+    // (it waits for this grid to finish before reading any partial).
+    griddep_launch_dependents();
     if (dynamic && threadIdx.x == 0) finish_handouts(p.work_ctr);
 
     // A wait gave up: let copies still in flight land before the CTA exits.
@@ -754,6 +757,7 @@ constexpr int kReduceWarps = 8;
 
 template <typename OutT, int HD>
 __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
+    griddep_wait();   // the partition pass (launched before, programmatically) is done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qh = blockIdx.x;
     // Newest partials first when they do not all fit in L2: the partition pass
@@ -944,10 +948,23 @@ int launch_simt(const DecodeParams &p, long long items, int dev, cudaStream_t st
     return PA_OK;
 }
 
+// The merge is launched as a programmatic dependent of the partition pass: its
+// CTAs may become resident while the pass's last CTAs finish, and wait in
+// griddep_wait() until the pass is complete.  After any other kind of
+// predecessor it simply starts when that one has finished.
 template <typename OutT, int HD>
-void launch_reduce(const DecodeParams &p, cudaStream_t st) {
-    dim3 grid(p.num_q_heads, p.num_seqs);
-    pa::decode_reduce_kernel<OutT, HD><<<grid, pa::kReduceWarps * 32, 0, st>>>(p);
+cudaError_t launch_reduce(const DecodeParams &p, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_q_heads, p.num_seqs);
+    cfg.blockDim = dim3(pa::kReduceWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pa::decode_reduce_kernel<OutT, HD>, p);
 }
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -1087,13 +1104,12 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     }
     if (rc != PA_OK) return rc;
     if (max_parts > 1 && a->phase != PA_PHASE_PARTITIONS) {
-        if (a->dtype == PA_BF16) {
-            if (head_dim == 128) launch_reduce<__nv_bfloat16, 128>(p, st);
-            else launch_reduce<__nv_bfloat16, 64>(p, st);
-        } else {
-            if (head_dim == 128) launch_reduce<float, 128>(p, st);
-            else launch_reduce<float, 64>(p, st);
-        }
+        cudaError_t le;
+        if (a->dtype == PA_BF16)
+            le = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128>(p, st) : launch_reduce<__nv_bfloat16, 64>(p, st);
+        else
+            le = head_dim == 128 ? launch_reduce<float, 128>(p, st) : launch_reduce<float, 64>(p, st);
+        if (le != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(le));
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));

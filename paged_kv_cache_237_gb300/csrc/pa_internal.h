@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Programmatic dependent launch.  A kernel that ends with work for the next
+// launch in its stream lets that launch start early with
+// griddep_launch_dependents(); the dependent kernel calls griddep_wait()
+// before it reads anything the first one wrote: the wait returns once the
+// kernels it depends on have finished and their writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Untiled bulk copy global -> shared (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
