@@ -911,7 +911,6 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
     return r == CUDA_SUCCESS;
 }
 
-
 template <typename T>
 constexpr int simt_stages() { return sizeof(T) == 4 ? 2 : 3; }
 
