@@ -349,3 +349,29 @@ def test_work_counter_survives_phases_graphs_and_size_changes(pa):
         torch.cuda.synchronize()
         assert status.read() == 0 and int(ws[:8].view(torch.int64).item()) == 0
         assert_decode_close(d, ref, torch.bfloat16, what=f"P={P} after other sizes")
+
+
+def test_loose_max_context_len_leaves_most_ctas_without_work(pa):
+    """max_context_len far above the real lengths: the host's bound on work
+    items (and so the grid) is much larger than the items that exist, so most
+    CTAs find no item at all.  They must still report finishing, so the work
+    counter is back at zero, and every row matches the oracle, call after
+    call."""
+    lens = [5, 700, 33, 1]
+    width = 4096                                   # table room for 65,536 tokens at bs 16
+    q, kc, vc, tables, lens_t = make_case(lens, 16, 2, 128, 16, torch.bfloat16, seed=41)
+    wide = torch.full((len(lens), width), -1, dtype=torch.int32, device="cuda")
+    wide[:, :tables.shape[1]] = tables
+    max_ctx = 65536
+    need = pa.pa_decode_workspace_size(len(lens), 16, 128, max_ctx, 512)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 0.1)
+    for skip in (False, True, True):
+        out = torch.empty_like(q)
+        status = pa.DeviceStatus()
+        pa.pa_decode(out, q, kc, vc, wide, lens_t, 0.1, max_context_len=max_ctx, partition_size=512,
+                     workspace=ws, status=status, skip_counter_reset=skip)
+        torch.cuda.synchronize()
+        assert status.read() == 0
+        assert int(ws[:8].view(torch.int64).item()) == 0
+        assert_decode_close(out, ref, torch.bfloat16, what=f"loose max_context_len, skip={skip}")
