@@ -71,3 +71,61 @@ def test_multi_step_serving_loop_matches_the_oracle():
         ref = oracle.paged_decode(q, kc_h, vc_h, tables, lens, scale)
         assert_decode_close(out, ref, torch.bfloat16, what=f"serving step {step}")
     assert torch.equal(bits(kc.cpu()), bits(kc_h)) and torch.equal(bits(vc.cpu()), bits(vc_h))
+
+
+def test_serving_loop_with_a_sequence_swapped_out_and_back_in():
+    """A sequence leaves the device mid-loop (its blocks moved to a pinned host
+    pool with pa_swap_blocks), sits out two steps while its device blocks are
+    reused, comes back into fresh device blocks, and decodes on: every step
+    matches the oracle, and both pools match their host truth bit for bit."""
+    from paged_kv_cache_237_gb300 import binding
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    rng = np.random.default_rng(23)
+    nb, nb_host, bs, Hq, Hkv, hd, scale = 160, 64, 16, 16, 2, 128, 0.09
+    g = torch.Generator().manual_seed(23)
+    kc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(torch.bfloat16)
+    vc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(torch.bfloat16)
+    kc, vc = kc_h.cuda(), vc_h.cuda()
+    hk = torch.zeros(nb_host, Hkv, bs, hd, dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros(nb_host, Hkv, bs, hd, dtype=torch.bfloat16).pin_memory()
+    hk_h, hv_h = hk.clone(), hv.clone()
+    dev, host = binding.BlockManager(nb, bs), binding.BlockManager(nb_host, bs)
+    prompt = rng.integers(0, 30000, size=400).tolist()
+    live = []
+    for sid in range(3):                               # prefix-cached: their prompt blocks are shared
+        dev.add_seq_cached(sid, prompt + rng.integers(0, 30000, size=int(rng.integers(1, 40))).tolist(), salt=0)
+        live.append(sid)
+    for sid in (3, 4):                                 # private sequences: movable
+        dev.add_seq(sid, int(rng.integers(100, 300)))
+        live.append(sid)
+    status = binding.DeviceStatus()
+    moved = 4
+    for step in range(7):
+        if step == 2:                                  # swap out: device -> pinned host
+            pairs = dev.move_seq(host, moved)
+            binding.pa_swap_blocks(kc, vc, hk, hv, pairs.cuda(), status=status)
+            oracle.swap_blocks(kc_h, vc_h, hk_h, hv_h, pairs)
+            live.remove(moved)
+        if step == 5:                                  # swap back in, to whatever device blocks are free
+            pairs = host.move_seq(dev, moved)
+            binding.pa_swap_blocks(hk, hv, kc, vc, pairs.cuda(), status=status)
+            oracle.swap_blocks(hk_h, hv_h, kc_h, vc_h, pairs)
+            live.append(moved)
+        seqs = list(live)
+        slots, cow = dev.append_slots(seqs)
+        tables, lens = dev.build_tables(seqs, max(len(dev.block_table(s)) for s in seqs))
+        q = torch.randn(len(seqs), Hq, hd, generator=g).to(torch.bfloat16)
+        kn = torch.randn(len(seqs), Hkv, hd, generator=g).to(torch.bfloat16)
+        vn = torch.randn(len(seqs), Hkv, hd, generator=g).to(torch.bfloat16)
+        dstep = DecodeStep(q.cuda(), kc, vc, tables.cuda(), lens.cuda(), scale, int(lens.max()), 128,
+                           status=status)
+        out = dstep.run_fused(kn.cuda(), vn.cuda(), slots.cuda(), cow.cuda() if cow.numel() else None)
+        torch.cuda.synchronize()
+        assert status.read() == 0, f"step {step}"
+        if cow.numel():
+            oracle.copy_blocks(kc_h, vc_h, cow)
+        oracle.reshape_and_cache(kn, vn, kc_h, vc_h, slots)
+        ref = oracle.paged_decode(q, kc_h, vc_h, tables, lens, scale)
+        assert_decode_close(out, ref, torch.bfloat16, what=f"swap loop step {step}")
+    assert torch.equal(bits(kc.cpu()), bits(kc_h)) and torch.equal(bits(vc.cpu()), bits(vc_h))
+    assert torch.equal(bits(hk), bits(hk_h)) and torch.equal(bits(hv), bits(hv_h))
