@@ -59,8 +59,6 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_paged_decode.restype = i32
     lib.oracle_paged_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                         i32, i32, dbl, vp, i64, i32]
-    lib.oracle_attention_contiguous.restype = i32
-    lib.oracle_attention_contiguous.argtypes = [vp, vp, vp, vp, i32, i32, dbl]
     lib.oracle_reshape_and_cache.restype = i32
     lib.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     lib.oracle_copy_blocks.restype = i32
@@ -132,20 +130,6 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                  _cache_dtype(kc), bt.data_ptr(), bt.shape[1], cl.data_ptr(),
                                  S, Hq, Hkv, hd, bs, nb, float(scale), pp, npairs, nthreads)
     _check(rc, "paged_decode")
-    return out
-
-
-def attention_contiguous(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float,
-                         lib: ctypes.CDLL | None = None) -> torch.Tensor:
-    """fp64 attention of one query row q [hd] over contiguous K, V [n, hd]."""
-    lib = lib or load()
-    q64 = q.to(torch.float64).contiguous()
-    K64 = K.to(torch.float64).contiguous()
-    V64 = V.to(torch.float64).contiguous()
-    out = torch.empty(q64.shape[-1], dtype=torch.float64)
-    rc = lib.oracle_attention_contiguous(out.data_ptr(), q64.data_ptr(), K64.data_ptr(),
-                                         V64.data_ptr(), K64.shape[0], q64.shape[-1], float(scale))
-    _check(rc, "attention_contiguous")
     return out
 
 

@@ -56,7 +56,3 @@ def decode_algorithmic_bytes(context_lens, num_q_heads: int, num_kv_heads: int, 
     tables = sum(blocks_for_tokens(n, block_size) for n in context_lens) * 4
     return kv + qo + tables + len(context_lens) * 4
 
-
-def ceil_div(a: int, b: int) -> int:
-    return -(-a // b)
-

@@ -240,21 +240,6 @@ int oracle_paged_decode(double *out, const double *q, const void *k_cache,
     return ORACLE_OK;
 }
 
-/* Attention of one query row over contiguous K, V (fp64), exposed so the
- * tests can check the textbook step on its own. */
-int oracle_attention_contiguous(double *out, const double *q, const double *K,
-                                const double *V, int n, int head_dim, double scale)
-{
-    if (!out || !q || n < 0 || head_dim <= 0 || (n > 0 && (!K || !V)))
-        return ORACLE_ERR_ARG;
-    double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-    if (!s)
-        return ORACLE_ERR_NOMEM;
-    attend_contiguous(out, q, K, V, n, head_dim, scale, s);
-    free(s);
-    return ORACLE_OK;
-}
-
 /* Cache write: token t's K and V rows (all KV heads) go to physical slot
  * slot_mapping[t] = block * block_size + offset; a negative slot is padding
  * and is skipped.  Plain byte copies of elem_bytes-wide elements.
