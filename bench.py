@@ -40,13 +40,15 @@ L2_BYTES = 129 * 2**20
 
 # DRAM read+write bytes of one partition-pass launch (with the fused cache
 # write), per workload, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
-# (a one-pass capture) of that workload's own launch: the long-context launch at
-# full size (profiles/decode_bf16_kernel_long_context.md), the GQA batch
-# (profiles/decode_bf16_kernel_gqa_llama3_70b.md).  Valid only while the kernel
-# source is the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "88d26b8f68a9cc31",
-                   "bytes_per_launch": {"long_context": 20801741824 + 297158144,
-                                        "gqa_llama3_70b": 902382592 + 6171648}}
+# on one launch.  Captures stay small (a few GB on the device): the GQA batch is
+# captured whole (0.9 GB of K/V); the long-context figure is a capture of a
+# seeded slice of the same length mix (--num-seqs), scaled to the full launch
+# by the ratio of algorithmic bytes.  Valid only while the kernel source is
+# the one captured.
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "cc4cbf6d384692de",
+                   # 48-sequence slice: 4,143,344,640 B read + 26,897,920 B written
+                   # over 4,141,526,704 algorithmic bytes, scaled to 20,791,665,640
+                   "bytes_per_launch": {"long_context": 20935827568}}
 
 
 def kernel_source(*texts: bytes) -> bytes:
@@ -110,6 +112,27 @@ def partition_pass_bytes(lens, num_q_heads, num_kv_heads, head_dim, block_size, 
             + sum(-(-n // block_size) for n in lens) * 4 + 4 * len(lens))
 
 
+NOMINAL_HBM_GBPS = 7900.0     # GB300 HBM3e, datasheet figure
+
+
+def fractions(gbps: float, peak: float) -> dict:
+    """A bandwidth as a fraction of the measured copy peak (the roofline
+    denominator; a read-only stream may exceed it, since a copy also writes)
+    and of the datasheet HBM bandwidth."""
+    return {"of_measured_copy_peak": round(gbps / peak, 4),
+            "of_datasheet_7900_GBps": round(gbps / NOMINAL_HBM_GBPS, 4)}
+
+
+def load_peak():
+    """(HBM copy peak in GB/s, 'measured' | 'fallback')."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
 # ---------------------------------------------------------------- clocks ---
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -160,9 +183,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- workloads ---
-def build_workload(name: str, device, seed_offset: int, gqa_sigma: float = 1.0):
+def build_workload(name: str, device, seed_offset: int, gqa_sigma: float = 1.0, num_seqs=None):
     from paged_kv_cache_237_gb300 import engine, workloads
     if name == "prefix_share":
+        if num_seqs is not None:
+            raise ValueError("--num-seqs does not apply to the prefix-sharing batch")
         st = engine.prefix_share_state(device, seed=workloads.WORKLOADS[name].seed + seed_offset)
         w = st["workload"]
         d = dict(workload=w, q=st["q"], k_cache=st["k_cache"], v_cache=st["v_cache"],
@@ -172,7 +197,7 @@ def build_workload(name: str, device, seed_offset: int, gqa_sigma: float = 1.0):
                  max_context_len=st["max_context_len"])
     else:
         d = workloads.decode_inputs(name, device=device, seed=workloads.WORKLOADS[name].seed + seed_offset,
-                                    gqa_sigma=gqa_sigma)
+                                    gqa_sigma=gqa_sigma, num_seqs=num_seqs)
         d["cow_pairs"] = None
     return d
 
@@ -294,13 +319,22 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_context",
-                    choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context"])
+                    choices=["tiny_f32", "mha_llama2_7b", "gqa_llama3_70b", "prefix_share", "long_context",
+                             "mha_llama2_7b_f32", "gqa_llama3_70b_f32"])
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="keep only the first N sequences of the drawn batch (a smaller slice of the same "
+                         "length mix, for profiler captures)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run the warm-up steps and one more step of the workload, print nothing and exit: "
+                         "a short program for profiler captures (the last step's partition pass is launch "
+                         "number 2 * (warmup + 1) of decode_*_kernel and the merge kernel together)")
     ap.add_argument("--gqa-sigma", type=float, default=1.0,
                     help="log-space spread of the GQA batch's lognormal lengths (1.0; 0.5 is the sensitivity case)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the same-run measurement of the GQA Llama-3-70B-shaped batch")
+                    help="skip the same-run measurements of the other workloads, the placement study and "
+                         "the cache-op sizes")
     ap.add_argument("--simt", action="store_true",
                     help="bf16 products on plain fp32 FMAs (SIMT kernel) instead of tensor-core MMAs")
     ap.add_argument("--unfused", action="store_true",
@@ -355,7 +389,7 @@ def main():
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    d = build_workload(args.workload, device, seed_offset=rank, gqa_sigma=args.gqa_sigma)
+    d = build_workload(args.workload, device, seed_offset=rank, gqa_sigma=args.gqa_sigma, num_seqs=args.num_seqs)
     w = d["workload"]
     elem = torch.tensor([], dtype=w.dtype).element_size()
     lens = d["lens"]
@@ -403,6 +437,14 @@ def main():
     torch.cuda.synchronize(device)
     if step.status.read():
         raise RuntimeError("device status flagged an input error")
+    if args.profile:
+        one_step(stream)
+        torch.cuda.synchronize(device)
+        if step.status.read():
+            raise RuntimeError("device status flagged an input error")
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     # The timed step is a CUDA graph of the step's launches (how a decode loop
     # runs in production): replays leave no host gaps between kernels, so the
@@ -549,25 +591,30 @@ def main():
                "single_core_value": round(sample_kv_bytes(d, one) / dt1 / 1e9, 4),
                "single_core_sample": f"{len(one)} sequences, 1 thread, {dt1:.1f} s"}
 
-    secondary = None
-    if rank == 0 and world == 1 and args.workload == "long_context" and not args.no_secondary:
+    secondary = placement = cache_ops = None
+    peak, peak_src = load_peak()
+    if rank == 0 and world == 1 and args.workload == "long_context" and args.num_seqs is None \
+            and not args.no_secondary:
+        # every other workload's step, in the same run (the long-context batch is the line's own)
         n2 = max(args.steps, 100)
-        secondary = {"gqa_llama3_70b": measure_step("gqa_llama3_70b", n2),
-                     "gqa_llama3_70b_sigma0.5": measure_step("gqa_llama3_70b", n2, gqa_sigma=0.5)}
+        secondary = {}
+        for key, name, sigma in (("tiny_f32", "tiny_f32", 1.0), ("mha_llama2_7b", "mha_llama2_7b", 1.0),
+                                 ("gqa_llama3_70b", "gqa_llama3_70b", 1.0),
+                                 ("gqa_llama3_70b_sigma0.5", "gqa_llama3_70b", 0.5),
+                                 ("prefix_share", "prefix_share", 1.0),
+                                 ("mha_llama2_7b_f32", "mha_llama2_7b_f32", 1.0),
+                                 ("gqa_llama3_70b_f32", "gqa_llama3_70b_f32", 1.0)):
+            secondary[key] = measure_step(name, n2, gqa_sigma=sigma, peak=peak)
+        # the pages' gather-overhead figures, measured on this kernel
+        placement = placement_block("long_context", 40, args.warmup)
+        # cache write and block copy at a decode step's size and at streaming sizes
+        cache_ops = cache_ops_block(100, args.warmup, tokens=(256, 65536), pairs=(24, 2048))
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
 
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     part_avg = statistics.mean(part_ms)
     achieved = B_part / (part_avg * 1e-3) / 1e9
     value = B_job / (ms * 1e-3) / 1e9
@@ -586,7 +633,7 @@ def main():
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
         "config": workload_config(w, d, world, args.gqa_sigma),
-        "hbm_fraction": round(B / (ms * 1e-3) / 1e9 / peak, 4),
+        "hbm_fraction": fractions(B / (ms * 1e-3) / 1e9, peak),
         "page_granular": {"bytes_per_step": B_pages, "GBps": round(B_pages / (ms * 1e-3) / 1e9, 2),
                           "what": "K/V counted by whole pages (partial last blocks in full)"},
         "seq_layer_steps_per_s": round(world * len(lens) / (ms * 1e-3), 1),
@@ -598,6 +645,7 @@ def main():
                       "partition_pass": round(part_avg, 4), "split_k_reduce": round(statistics.mean(red_ms), 4)},
         "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel (partition pass)"
                      if w.dtype == torch.bfloat16 and not args.simt else "decode_simt_kernel (partition pass)",
+                     "peak_what": "HBM copy bandwidth (read + write), so a read-only stream may exceed 1",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "bytes_per_launch": B_part,
@@ -619,10 +667,11 @@ def main():
         line["unique_kv_bytes"] = uniq
         line["unique_kv_GBps"] = round(uniq / (ms * 1e-3) / 1e9, 1)
     if secondary is not None:
-        for v in secondary.values():
-            v["hbm_fraction"] = round(v["value"] / peak, 4)
-            v["partition_pass_frac"] = round(v["partition_pass_GBps"] / peak, 4)
         line["secondary_workloads"] = secondary
+    if placement is not None:
+        line["placement"] = placement
+    if cache_ops is not None:
+        line["cache_ops"] = cache_ops
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -650,15 +699,12 @@ def time_partition_pass(d, steps: int, warmup: int) -> float:
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-def run_placement_study(args):
+def placement_block(name: str, steps: int, warmup: int) -> dict:
     """Gather overhead and block-size trade-off on the same kernel: the
-    partition pass over the long-context lengths with every sequence's blocks
-    shuffled across the pool or laid out consecutively, at block size 32 and 16."""
-    from paged_kv_cache_237_gb300 import build as pa_build
+    partition pass over one workload's lengths with every sequence's blocks
+    shuffled across the pool or laid out consecutively, at block size 32 and
+    16 (CUDA events, mean of `steps` launches)."""
     from paged_kv_cache_237_gb300 import workloads
-    pa_build.build()
-    torch.cuda.set_device(0)
-    name = args.workload
     rows = {}
     for bs in (32, 16):
         for shuffle in (True, False):
@@ -666,18 +712,26 @@ def run_placement_study(args):
             w = d["workload"]
             e = torch.tensor([], dtype=w.dtype).element_size()
             B = partition_pass_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, bs, e, e)
-            ms = time_partition_pass(d, args.steps, args.warmup)
+            ms = time_partition_pass(d, steps, warmup)
             rows[f"bs{bs}_{'shuffled' if shuffle else 'identity'}"] = {
                 "ms": round(ms, 4), "GBps": round(B / (ms * 1e-3) / 1e9, 1),
                 "table_entries": int(sum(-(-int(n) // bs) for n in d["lens"]))}
             del d
             torch.cuda.empty_cache()
-    out = {"study": "placement", "workload": name, "steps": args.steps, "kernel": "partition pass",
-           "results": rows,
-           "gather_overhead_bs32": round(rows["bs32_shuffled"]["ms"] / rows["bs32_identity"]["ms"] - 1, 4),
-           "gather_overhead_bs16": round(rows["bs16_shuffled"]["ms"] / rows["bs16_identity"]["ms"] - 1, 4),
-           "bs16_vs_bs32_shuffled": round(rows["bs16_shuffled"]["ms"] / rows["bs32_shuffled"]["ms"] - 1, 4)}
-    print(json.dumps(out), flush=True)
+    return {"workload": name, "steps": steps, "kernel": "partition pass", "results": rows,
+            "gather_overhead_bs32": round(rows["bs32_shuffled"]["ms"] / rows["bs32_identity"]["ms"] - 1, 4),
+            "gather_overhead_bs16": round(rows["bs16_shuffled"]["ms"] / rows["bs16_identity"]["ms"] - 1, 4),
+            "bs16_vs_bs32_shuffled": round(rows["bs16_shuffled"]["ms"] / rows["bs32_shuffled"]["ms"] - 1, 4),
+            "what": "partition pass with blocks shuffled across the pool vs laid out consecutively; "
+                    "overhead = shuffled / identity time - 1"}
+
+
+def run_placement_study(args):
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    torch.cuda.set_device(0)
+    print(json.dumps({"study": "placement", **placement_block(args.workload, args.steps, args.warmup)}),
+          flush=True)
 
 
 def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_len: int = 2048):
@@ -811,19 +865,16 @@ def run_swap_study(args, num_blocks: int = 4096):
           flush=True)
 
 
-def run_cache_ops_study(args):
+def cache_ops_block(steps: int, warmup: int, tokens=(256, 4096, 65536), pairs=(24, 256, 2048)) -> dict:
     """pa_reshape_and_cache and pa_copy_blocks at decode-step sizes (latency)
     and at sizes where they stream HBM: the long-context geometry (8 KV heads,
     block_size 32, head_dim 128, bf16), distinct random slots and pairs, CUDA
     graphs of single launches, inputs larger than L2 where the size allows
     (a 512 MB buffer is written between launches otherwise).  Bytes are read +
     written bytes of the cache rows or blocks moved."""
-    from paged_kv_cache_237_gb300 import build as pa_build
-    pa_build.build()
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.workloads import randn
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     Hkv, bs, hd = 8, 32, 128
     pool = 40000                                  # 2.6 GB per cache
     kc = randn((pool, Hkv, bs, hd), torch.bfloat16, 91, dev)
@@ -832,22 +883,16 @@ def run_cache_ops_study(args):
     status = binding.DeviceStatus(dev)
     stream = torch.cuda.current_stream()
     rng = np.random.default_rng(13)
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak, _ = load_peak()
 
     def timed(fn, flush_between):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):          # fn launches on the current (capturing) stream
             fn()
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in ev:
             a.record(stream)
             g.replay()
@@ -858,7 +903,7 @@ def run_cache_ops_study(args):
         return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     rows = {}
-    for T in (256, 4096, 65536):
+    for T in tokens:
         k = randn((T, Hkv, hd), torch.bfloat16, 93, dev)
         v = randn((T, Hkv, hd), torch.bfloat16, 94, dev)
         slots = torch.from_numpy(rng.choice(pool * bs, size=T, replace=False).astype(np.int64)).to(dev)
@@ -867,42 +912,74 @@ def run_cache_ops_study(args):
                    nbytes < 2 * L2_BYTES)
         rows[f"reshape_and_cache_T{T}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
                                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
-    for P in (24, 256, 2048):
+    for P in pairs:
         ids = rng.choice(pool, size=2 * P, replace=False)
-        pairs = torch.from_numpy(np.stack([ids[:P], ids[P:]], 1).astype(np.int64)).to(dev)
+        pr = torch.from_numpy(np.stack([ids[:P], ids[P:]], 1).astype(np.int64)).to(dev)
         nbytes = P * 2 * Hkv * bs * hd * 2 * 2 + P * 16
-        ms = timed(lambda: binding.pa_copy_blocks(kc, vc, pairs, status=status),
+        ms = timed(lambda: binding.pa_copy_blocks(kc, vc, pr, status=status),
                    nbytes < 2 * L2_BYTES)
         rows[f"copy_blocks_P{P}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
                                      "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
     if status.read():
         raise RuntimeError("device status flagged an input error")
-    print(json.dumps({"study": "cache_ops", "geometry": "8 KV heads, block_size 32, head_dim 128, bf16",
-                      "peak_GBps": peak, "results": rows}), flush=True)
+    del kc, vc, flush
+    torch.cuda.empty_cache()
+    return {"geometry": "8 KV heads, block_size 32, head_dim 128, bf16", "peak_GBps": peak,
+            "frac_of": "measured copy peak", "results": rows}
 
 
-def measure_step(name: str, steps: int, warmup: int = 5, gqa_sigma: float = 1.0) -> dict:
-    """Graph-replayed decode step (fused cache write + merge) of another
-    workload, timed in the same run: step GB/s and the partition pass alone."""
+def run_cache_ops_study(args):
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    torch.cuda.set_device(0)
+    print(json.dumps({"study": "cache_ops", **cache_ops_block(args.steps, args.warmup)}), flush=True)
+
+
+def measure_step(name: str, steps: int, warmup: int = 5, gqa_sigma: float = 1.0, peak: float | None = None,
+                 simt: bool = False) -> dict:
+    """Graph-replayed decode step of another workload, timed in the same run:
+    step GB/s and the partition pass alone.  The step is the one the main line
+    times (copy-on-write copies, the decode launch with the fused cache write,
+    the split-K merge); a workload whose writes are not each sequence's last
+    position (the tiny fp32 batch) writes them with a separate launch.  Inputs
+    smaller than twice L2 get a 512 MB write between replays, outside the
+    events."""
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.engine import DecodeStep
-    d = build_workload(name, torch.device("cuda", torch.cuda.current_device()), 0, gqa_sigma)
+    from paged_kv_cache_237_gb300.workloads import new_token_slots
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = build_workload(name, dev, 0, gqa_sigma)
     w = d["workload"]
     e = torch.tensor([], dtype=w.dtype).element_size()
-    B = decode_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e, e)
-    Bp = partition_pass_bytes(d["lens"], w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e)
+    lens = d["lens"]
+    B = decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e, e)
+    Bp = partition_pass_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, e, e)
     step = DecodeStep(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], d["scale"],
-                      d["max_context_len"], w.partition_size)
+                      d["max_context_len"], w.partition_size, simt=simt)
+    last = new_token_slots(lens, d["block_tables"].cpu().numpy(), w.block_size)
+    fused = (d["slot_mapping"].numel() == len(lens)
+             and bool(np.array_equal(last, d["slot_mapping"].cpu().numpy())))
     tok = (d["k_new"], d["v_new"], d["slot_mapping"])
+    cow = d["cow_pairs"]
+    working_set = d["k_cache"].numel() * e * 2
+    flush = None if working_set > 2 * L2_BYTES else torch.empty(512 * 2**20 // 4, dtype=torch.float32,
+                                                                  device=dev)
 
     def full(_):
-        step.run_fused(*tok, d["cow_pairs"])
+        if fused:
+            step.run_fused(*tok, cow)
+        else:
+            step.run(*tok, cow)
 
     def part(_):
-        step.decode(None, binding.PA_PHASE_PARTITIONS, *tok)
+        if fused:
+            step.decode(None, binding.PA_PHASE_PARTITIONS, *tok)
+        else:
+            step.decode(None, binding.PA_PHASE_PARTITIONS)
 
     for _ in range(warmup):
         full(None)
+        flush_l2(flush)
     torch.cuda.synchronize()
     if step.status.read():
         raise RuntimeError("device status flagged an input error")
@@ -913,21 +990,43 @@ def measure_step(name: str, steps: int, warmup: int = 5, gqa_sigma: float = 1.0)
         with torch.cuda.graph(g, capture_error_mode="relaxed"):
             fn(None)
         g.replay()
+        flush_l2(flush)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in ev:
             a.record(stream)
             g.replay()
             b.record(stream)
+            flush_l2(flush)
         torch.cuda.synchronize()
         out[key] = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    tokens = int(sum(int(n) for n in d["lens"]))
-    del d, step
-    torch.cuda.empty_cache()
-    res = {"ms_per_step": round(out["step"], 4), "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
+    if step.status.read():
+        raise RuntimeError("device status flagged an input error")
+    res = {"dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+           "kernel": "decode_bf16_kernel" if w.dtype == torch.bfloat16 and not simt else "decode_simt_kernel",
+           "ms_per_step": round(out["step"], 4), "us_per_step": round(out["step"] * 1e3, 2),
+           "value": round(B / (out["step"] * 1e-3) / 1e9, 1),
+           "partition_pass_ms": round(out["partition_pass"], 4),
            "partition_pass_GBps": round(Bp / (out["partition_pass"] * 1e-3) / 1e9, 1),
-           "total_context_tokens": tokens}
-    if name == "gqa_llama3_70b":
+           "bytes_per_step": int(B), "total_context_tokens": int(sum(int(n) for n in lens)),
+           "l2": "inputs larger than L2 (no flush)" if flush is None else "512 MB L2 flush between steps"}
+    if peak:
+        res["hbm_fraction"] = fractions(res["value"], peak)
+        res["partition_pass_frac"] = round(res["partition_pass_GBps"] / peak, 4)
+    if name.startswith("gqa_llama3_70b"):
         res["lognormal_sigma"] = gqa_sigma
+    if cow is not None:
+        # prefix sharing: the logical figure counts the shared prompt once per
+        # sequence (it is read from L2 after the first); this one counts the
+        # distinct blocks the step reads
+        bs = w.block_size
+        tab = d["block_tables"].cpu().numpy()
+        used = {int(b) for i, n in enumerate(lens) for b in tab[i, :-(-int(n) // bs)]}
+        uniq = len(used) * w.num_kv_heads * bs * w.head_dim * 2 * e
+        res["copy_on_write_pairs"] = int(cow.numel() // 2)
+        res["unique_kv_bytes"] = uniq
+        res["unique_kv_GBps"] = round(uniq / (out["step"] * 1e-3) / 1e9, 1)
+    del d, step, flush
+    torch.cuda.empty_cache()
     return res
 
 

@@ -108,7 +108,13 @@ typedef struct pa_decode_args {
                                bytes, then the split-K partials; may be NULL
                                when max_context_len <= partition_size.  No
                                part needs to start at zero (see
-                               skip_counter_reset). */
+                               skip_counter_reset).  One workspace serves one
+                               call at a time: two calls that may run at the
+                               same time on the GPU (different streams with no
+                               ordering between them) must not share it, since
+                               they would race on its work counter and
+                               partials.  Calls ordered on one stream may
+                               share it. */
     size_t workspace_bytes; /* >= pa_decode_workspace_size(...) */
     int32_t *dev_status;    /* optional device word for PA_STATUS_* bits */
     void *stream;           /* cudaStream_t */
@@ -181,7 +187,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
  *    are rejected with PA_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device that needs the scratch looks up its device
  *    address (cudaGetSymbolAddress) with that device current; make that first
- *    call before any stream capture on the device.
+ *    call before any stream capture on the device.  The address is kept for
+ *    the life of the process: after cudaDeviceReset (or anything else that
+ *    destroys the device's primary context) it is stale, and this call must
+ *    not be used on that device again.
+ *  - Arguments are checked as pa_decode checks them, before the scratch is
+ *    sized; a bad partition_size, block_size or head_dim gives the same code
+ *    as there.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents; no part of it needs to start at zero (each call writes every
  *    partial it reads, and the work counter is reset before each pass unless

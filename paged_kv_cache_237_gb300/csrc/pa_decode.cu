@@ -983,20 +983,20 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int he
                                            int max_context_len, int partition_size) {
     const int P = effective_partition(partition_size);
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len <= 0 || P <= 0) return 0;
-    const long long max_parts = (max_context_len + P - 1) / P;
+    const long long max_parts = (static_cast<long long>(max_context_len) + P - 1) / P;
     if (max_parts <= 1) return 0;
     const size_t rows = static_cast<size_t>(num_seqs) * max_parts * num_q_heads;
     return kWorkspaceHeader + align256(rows * 2 * sizeof(float)) + align256(rows * head_dim * sizeof(float));
 }
 
-extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                         const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
-                         int num_kv_heads, int head_dim, int block_size, float scale,
-                         const pa_decode_args *a) {
-    PaTraceRange trace("pa_decode");
-    if (!a) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: args is NULL");
-    if (a->num_seqs < 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs < 0");
-    if (a->num_seqs == 0) return PA_OK;
+namespace {
+
+// Argument checks shared by pa_decode and pa_decode_noalloc (everything but
+// the workspace), so both entry points give the same code for the same
+// mistake.  Called with num_seqs > 0.
+int check_decode_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, const pa_decode_args *a) {
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: null tensor pointer");
     if (a->dtype != PA_F32 && a->dtype != PA_BF16) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: bad dtype");
@@ -1020,10 +1020,32 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
         return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: k_new/v_new must be 16-byte and slot_mapping 8-byte aligned");
     const long long total_rows = static_cast<long long>(a->num_blocks) * num_kv_heads * block_size;
     if (total_rows >= INT_MAX) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: cache has 2^31 or more rows");
+    return PA_OK;
+}
 
+// Tokens a sequence can hold: max_context_len, bounded by the table's width.
+int context_cap(const pa_decode_args *a, int block_size) {
     const long long table_cap = static_cast<long long>(a->max_blocks_per_seq) * block_size;
-    const int ctx_cap = static_cast<int>(a->max_context_len < table_cap ? a->max_context_len : table_cap);
-    const int max_parts = ctx_cap <= P ? 1 : (ctx_cap + P - 1) / P;
+    return static_cast<int>(a->max_context_len < table_cap ? a->max_context_len : table_cap);
+}
+
+}  // namespace
+
+extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, float scale,
+                         const pa_decode_args *a) {
+    PaTraceRange trace("pa_decode");
+    if (!a) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: args is NULL");
+    if (a->num_seqs < 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs < 0");
+    if (a->num_seqs == 0) return PA_OK;
+    const int arc = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, num_q_heads,
+                                      num_kv_heads, head_dim, block_size, a);
+    if (arc != PA_OK) return arc;
+    const int P = effective_partition(a->partition_size);
+    const long long total_rows = static_cast<long long>(a->num_blocks) * num_kv_heads * block_size;
+    const int ctx_cap = context_cap(a, block_size);
+    const int max_parts = ctx_cap <= P ? 1 : static_cast<int>((static_cast<long long>(ctx_cap) + P - 1) / P);
     DecodeParams p{};
     if (max_parts > 1) {
         const size_t need = pa_decode_workspace_size(a->num_seqs, num_q_heads, head_dim, ctx_cap, P);
@@ -1157,10 +1179,15 @@ extern "C" int pa_decode_noalloc(void *out, const void *q, const void *k_cache, 
                                  const pa_decode_args *args) {
     PaTraceRange trace("pa_decode_noalloc");
     if (!args) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode_noalloc: args is NULL");
+    if (args->num_seqs < 0) return pa_fail(PA_ERR_INVALID_ARG, "pa_decode_noalloc: num_seqs < 0");
     if (args->num_seqs == 0) return PA_OK;
+    // The same checks as pa_decode first, so that a bad size is reported as
+    // such and not as a scratch too small for it.
+    const int arc = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, num_q_heads,
+                                      num_kv_heads, head_dim, block_size, args);
+    if (arc != PA_OK) return arc;
     const int P = effective_partition(args->partition_size);
-    const long long table_cap = static_cast<long long>(args->max_blocks_per_seq) * block_size;
-    const int ctx_cap = static_cast<int>(args->max_context_len < table_cap ? args->max_context_len : table_cap);
+    const int ctx_cap = context_cap(args, block_size);
     const size_t need = pa_decode_workspace_size(args->num_seqs, num_q_heads, head_dim, ctx_cap, P);
     if (need > PA_NOALLOC_WORKSPACE_BYTES)
         return pa_fail(PA_ERR_WORKSPACE,

@@ -32,6 +32,11 @@ Workloads (sizes fixed here; the pages name the shapes only loosely):
     partitions of 512 tokens; the pool is sized so that the sequences fill
     ~96% of it, with blocks scattered at random.
 
+``mha_llama2_7b_f32``, ``gqa_llama3_70b_f32``
+    The MHA and GQA batches above with fp32 K/V, q and output: the same
+    seeds, so the same lengths and placement, and the values before rounding
+    to bf16.
+
 All values are N(0, 1) cast to the workload dtype.  Context lengths include the
 token written by the step (a decode step first writes the new token's K/V, then
 attends over every token present).
@@ -58,10 +63,15 @@ class Workload:
     seed: int = 0
     notes: str = ""
     extra: dict = field(default_factory=dict)
+    recipe: str = ""          # length and pool recipe, when it is another workload's
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def kind(self) -> str:
+        return self.recipe or self.name
 
 
 WORKLOADS = {
@@ -70,6 +80,10 @@ WORKLOADS = {
     "gqa_llama3_70b": Workload("gqa_llama3_70b", torch.bfloat16, 32, 64, 8, 128, 16, 512, 3),
     "prefix_share": Workload("prefix_share", torch.bfloat16, 50, 32, 8, 128, 16, 512, 4),
     "long_context": Workload("long_context", torch.bfloat16, 256, 64, 8, 128, 32, 512, 5),
+    "mha_llama2_7b_f32": Workload("mha_llama2_7b_f32", torch.float32, 64, 32, 32, 128, 16, 512, 2,
+                                  recipe="mha_llama2_7b"),
+    "gqa_llama3_70b_f32": Workload("gqa_llama3_70b_f32", torch.float32, 32, 64, 8, 128, 16, 512, 3,
+                                   recipe="gqa_llama3_70b"),
 }
 
 
@@ -78,14 +92,14 @@ def context_lengths(w: Workload, rng: np.random.Generator, gqa_sigma: float = 1.
     ``gqa_sigma`` is the log-space spread of the GQA batch's lognormal (the
     recipe leaves it open: 1.0 by default, 0.5 as a sensitivity case; the
     same normal draws are scaled, so both cases share one median)."""
-    if w.name == "tiny_f32":
+    if w.kind == "tiny_f32":
         return np.array([7, 16, 33, 50], dtype=np.int64)
-    if w.name == "mha_llama2_7b":
+    if w.kind == "mha_llama2_7b":
         return rng.integers(128, 2048, size=w.num_seqs, endpoint=True).astype(np.int64)
-    if w.name == "gqa_llama3_70b":
+    if w.kind == "gqa_llama3_70b":
         z = rng.standard_normal(w.num_seqs)
         return np.clip(np.rint(4096.0 * np.exp(gqa_sigma * z)), 256, 32768).astype(np.int64)
-    if w.name == "long_context":
+    if w.kind == "long_context":
         short = rng.integers(16, 32768, size=w.num_seqs - 8, endpoint=True)
         lens = np.concatenate([np.full(8, 131072), short]).astype(np.int64)
         return lens[rng.permutation(w.num_seqs)]
@@ -94,13 +108,13 @@ def context_lengths(w: Workload, rng: np.random.Generator, gqa_sigma: float = 1.
 
 def pool_blocks(w: Workload, need: int) -> int:
     """Physical pool size for a workload needing `need` blocks."""
-    if w.name == "tiny_f32":
+    if w.kind == "tiny_f32":
         return 32
-    if w.name == "mha_llama2_7b":
+    if w.kind == "mha_llama2_7b":
         return math.ceil(1.2 * need)
-    if w.name == "gqa_llama3_70b":
+    if w.kind == "gqa_llama3_70b":
         return math.ceil(1.05 * need)
-    if w.name == "long_context":
+    if w.kind == "long_context":
         return math.ceil(need / 0.96)
     return need
 
@@ -150,7 +164,8 @@ def new_token_slots(lens: np.ndarray, tables: np.ndarray, block_size: int) -> np
 
 
 def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: bool = True,
-                  lens_override=None, block_size: int | None = None, gqa_sigma: float = 1.0) -> dict:
+                  lens_override=None, block_size: int | None = None, gqa_sigma: float = 1.0,
+                  num_seqs: int | None = None) -> dict:
     """All inputs of one decode step of a workload (except prefix_share).
 
     Returns a dict with q [S, Hq, hd], k_cache/v_cache [num_blocks, Hkv, bs, hd],
@@ -159,21 +174,25 @@ def decode_inputs(name: str, device="cpu", seed: int | None = None, shuffle: boo
     workload record and host copies of lengths and tables.  ``shuffle=False``
     places every sequence's blocks consecutively (identity placement);
     ``block_size`` overrides the workload's block size (same lengths, same
-    pool fill); ``gqa_sigma`` sets the GQA batch's lognormal spread.
+    pool fill); ``gqa_sigma`` sets the GQA batch's lognormal spread;
+    ``num_seqs`` keeps only the first sequences of the drawn batch (a smaller
+    slice of the same length mix, its pool sized by the same rule).
     """
     w = WORKLOADS[name]
     if block_size is not None and block_size != w.block_size:
         w = Workload(w.name, w.dtype, w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, block_size,
-                     w.partition_size, w.seed, w.notes, w.extra)
+                     w.partition_size, w.seed, w.notes, w.extra, w.recipe)
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     lens = context_lengths(w, rng, gqa_sigma) if lens_override is None else np.asarray(lens_override, np.int64)
+    if num_seqs is not None:
+        lens = lens[:num_seqs]
     need = sum((int(n) + w.block_size - 1) // w.block_size for n in lens)
     nb = pool_blocks(w, need)
     tables, _ = place_blocks(lens, w.block_size, nb, rng, shuffle=shuffle)
     S, Hq, Hkv, hd, bs = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     S = len(lens)
-    if name == "tiny_f32":
+    if w.kind == "tiny_f32":
         # four writes to distinct random slots of the 32-block pool
         slots = rng.choice(nb * bs, size=4, replace=False).astype(np.int64)
     else:

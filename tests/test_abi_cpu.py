@@ -90,3 +90,31 @@ def test_binding_refuses_cpu_tensors(lib):
         lib.pa_decode(q, q, torch.zeros(1, 2, 16, 64), torch.zeros(1, 2, 16, 64),
                       torch.zeros(1, 1, dtype=torch.int32), torch.ones(1, dtype=torch.int32), 0.1,
                       max_context_len=1)
+
+
+def test_workspace_size_at_the_largest_context_length(lib):
+    """The partition count is taken in 64 bits: a context bound of INT_MAX does
+    not overflow."""
+    int_max = 2**31 - 1
+    parts = -(-int_max // 512)
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(1, 1, 64, int_max, 512) == 256 + a256(parts * 8) + a256(parts * 64 * 4)
+    assert lib.pa_decode_workspace_size(1, 1, 64, int_max, 4096) == \
+        256 + a256(-(-int_max // 4096) * 8) + a256(-(-int_max // 4096) * 256)
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(partition_size=8), -1), (dict(partition_size=1), -1), (dict(partition_size=24), -1),
+    (dict(head_dim=96), -2), (dict(block_size=8), -2), (dict(dtype=7), -1), (dict(num_seqs=-1), -1),
+    (dict(max_context_len=1 << 20, partition_size=16), -7),
+])
+def test_noalloc_checks_arguments_before_sizing_its_scratch(lib, change, code):
+    """pa_decode_noalloc reports a bad size with the code pa_decode gives, not as
+    a scratch too small for it; only sizes that are valid but too large for its
+    fixed array get PA_ERR_WORKSPACE."""
+    a = _args(lib, num_seqs=change.get("num_seqs", 4), dtype=change.get("dtype", lib.PA_BF16),
+              partition_size=change.get("partition_size", 0),
+              max_context_len=change.get("max_context_len", 32768), max_blocks=1 << 16)
+    rc = lib._lib.pa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 8, change.get("head_dim", 128),
+                                    change.get("block_size", 16), 0.1, ctypes.byref(a))
+    assert rc == code, lib._lib.pa_last_error_string()
