@@ -51,10 +51,14 @@ TRAFFIC_CAPTURE = {"source_sha256_prefix": "cc4cbf6d384692de",
                    "bytes_per_launch": {"long_context": 20935827568}}
 
 
+KERNEL_FILES = ("pa_decode.cu", "pa_decode_common.cuh", "pa_internal.h")
+
+
 def kernel_source(*texts: bytes) -> bytes:
-    """The code the bf16 partition pass is built and launched from (pa_decode.cu
-    and pa_internal.h: kernels, helpers, launch shapes), with comments and
-    whitespace removed so that only code changes count."""
+    """The code the bf16 partition pass is built and launched from
+    (pa_decode.cu, pa_decode_common.cuh and pa_internal.h: kernels, helpers,
+    launch shapes), with comments and whitespace removed so that only code
+    changes count."""
     import re
     out = []
     for text in texts:
@@ -71,7 +75,7 @@ def captured_traffic(workload: str):
     csrc = os.path.join(ROOT, "paged_kv_cache_237_gb300", "csrc")
     try:
         texts = []
-        for name in ("pa_decode.cu", "pa_internal.h"):
+        for name in KERNEL_FILES:
             with open(os.path.join(csrc, name), "rb") as f:
                 texts.append(f.read())
         digest = hashlib.sha256(kernel_source(*texts)).hexdigest()[:16]

@@ -22,9 +22,9 @@ LIB_NAME = "libpa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["pa_decode.cu", "pa_cache.cu"]
+CUDA_SOURCES = ["pa_decode.cu", "pa_decode_simt.cu", "pa_cache.cu"]
 CXX_SOURCES = ["block_manager.cpp", "pa_api.cpp"]
-HEADERS = ["pa_internal.h"]
+HEADERS = ["pa_internal.h", "pa_decode_common.cuh"]
 
 
 def _nvcc() -> str:

@@ -28,8 +28,8 @@
 // heads) is the M dimension of mma.m16n8k16: S = Q K^T (tokens are N), the fp32
 // probabilities, split into a bf16 high part and a bf16 residual, feed
 // O += P_hi V + P_lo V directly from registers (two MMAs keep ~16 bits of p).
-// SIMT path (fp32 inputs, or bf16 on request): 1-D bulk copies and fp32 FMAs,
-// one lane per head_dim slice.
+// fp32 inputs (and bf16 on request) take a pass on plain fp32 FMAs instead,
+// pa_decode_simt.cu; the split-K merge below serves both.
 // Fused cache write (optional): the warp whose chunk holds a sequence's new
 // last token copies that row into its staged tile, and the CTA of query-head
 // tile 0 writes it to the caches, so one launch both writes and attends.
@@ -43,198 +43,9 @@
 #include <cstring>
 #include <mutex>
 
-#include "pa_internal.h"
+#include "pa_decode_common.cuh"
 
 namespace pa {
-
-__device__ __forceinline__ uint8_t *align_1024(uint8_t *p) {
-    uint32_t a = smem_addr(p);
-    return p + ((1024u - (a & 1023u)) & 1023u);
-}
-
-// Context length of sequence s, clamped into [0, ctx_cap].
-__device__ __forceinline__ int seq_len(const DecodeParams &p, int s) {
-    int n = p.context_lens[s];
-    return n < 0 ? 0 : (n > p.ctx_cap ? p.ctx_cap : n);
-}
-
-__device__ __forceinline__ int parts_of(int n, int P) { return n <= P ? 1 : (n + P - 1) / P; }
-
-// Position of the walk over (sequence, partition) pairs: `base` is the global
-// index of sequence `seq`'s first partition.
-struct SeqCursor {
-    int seq;
-    long long base;
-};
-
-// Move the cursor forward to the sequence that owns global partition gp
-// (32 sequences per step, warp-parallel).  False when gp is past the end.
-__device__ bool seek(SeqCursor &c, long long gp, const DecodeParams &p, int lane) {
-    while (c.seq < p.num_seqs) {
-        const int s = c.seq + lane;
-        const int np = s < p.num_seqs ? parts_of(seq_len(p, s), p.partition_size) : 0;
-        int incl = np;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const unsigned hit = __ballot_sync(kFull, s < p.num_seqs && gp < c.base + incl);
-        if (hit) {
-            const int L = __ffs(hit) - 1;
-            c.base += __shfl_sync(kFull, incl - np, L);
-            c.seq += L;
-            return true;
-        }
-        c.base += __shfl_sync(kFull, incl, 31);
-        c.seq += 32;
-    }
-    return false;
-}
-
-__device__ __forceinline__ void store4(float *dst, float4 v) { *reinterpret_cast<float4 *>(dst) = v; }
-
-__device__ __forceinline__ void store4(__nv_bfloat16 *dst, float4 v) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    memcpy(&u.x, &lo, 4);
-    memcpy(&u.y, &hi, 4);
-    *reinterpret_cast<uint2 *>(dst) = u;
-}
-
-// Merge the kWarps per-warp softmax states held in shared memory (each warp's
-// region starts with float O[16][HD + kEpiPad], then M[16], then L[16]) and
-// store either the final rows or the item's partial.
-template <typename OutT, int HD>
-__device__ void merge_and_store(const uint8_t *smem, int warp_bytes, const DecodeParams &p, int seq,
-                                int part, int qh0, int rows, bool single) {
-    constexpr int LD = HD + kEpiPad;
-    constexpr int Q4 = HD / 4;
-    for (int task = threadIdx.x; task < rows * Q4; task += blockDim.x) {
-        const int r = task / Q4, d = (task % Q4) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float *em = reinterpret_cast<const float *>(smem + w * warp_bytes) + 16 * LD;
-            M = fmaxf(M, em[r]);
-        }
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *eo = reinterpret_cast<const float *>(smem + w * warp_bytes);
-                const float f = exp2f(eo[16 * LD + r] - M);
-                L += f * eo[16 * LD + 16 + r];
-                const float4 v = *reinterpret_cast<const float4 *>(eo + r * LD + d);
-                acc.x += f * v.x;
-                acc.y += f * v.y;
-                acc.z += f * v.z;
-                acc.w += f * v.w;
-            }
-        }
-        const int qh = qh0 + r;
-        if (single) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            OutT *o = static_cast<OutT *>(p.out) + ((long long)seq * p.num_q_heads + qh) * HD + d;
-            store4(o, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-        } else {
-            const long long idx = ((long long)seq * p.max_parts + part) * p.num_q_heads + qh;
-            store4(p.part_acc + idx * HD + d, acc);
-            if (d == 0) *reinterpret_cast<float2 *>(p.part_ml + idx * 2) = make_float2(M, L);
-        }
-    }
-}
-
-// Describes the item a CTA is working on.
-struct Item {
-    int seq, part, kvh, ht, qh0, rows, n;
-    int tok_begin, tok_end, nchunks;
-    bool single;
-};
-
-__device__ __forceinline__ bool next_item(Item &it, SeqCursor &cur, long long item,
-                                          const DecodeParams &p, int tile_rows, int lane) {
-    const int T = p.num_kv_heads * p.head_tiles;
-    const long long gp = item / T;
-    if (!seek(cur, gp, p, lane)) return false;
-    const int r = static_cast<int>(item % T);
-    const int ht = r % p.head_tiles;
-    it.seq = cur.seq;
-    it.part = static_cast<int>(gp - cur.base);
-    it.kvh = r / p.head_tiles;
-    it.ht = ht;
-    it.qh0 = it.kvh * p.group + ht * tile_rows;
-    it.rows = min(tile_rows, p.group - ht * tile_rows);
-    const int raw = p.context_lens[it.seq];
-    if (threadIdx.x == 0 && r == 0 && it.part == 0 && (raw < 0 || raw > p.ctx_cap))
-        flag_status(p.status, PA_STATUS_BAD_CONTEXT_LEN);
-    const int n = seq_len(p, it.seq);
-    it.n = n;
-    it.tok_begin = it.part * p.partition_size;
-    it.tok_end = min(n, it.tok_begin + p.partition_size);
-    const int ntok = max(0, it.tok_end - it.tok_begin);
-    it.nchunks = (ntok + kChunk - 1) / kChunk;
-    it.single = n <= p.partition_size;
-    return true;
-}
-
-// Physical location of this warp's k-th chunk of the item, as a row of the
-// [num_blocks * Hkv * block_size, head_dim] view of a cache; an invalid block
-// id gives -1 and sets a flag (the bf16 path then loads rows past the view,
-// which TMA fills with zeros; the fp32 path skips the copy).
-__device__ __forceinline__ int chunk_row(const DecodeParams &p, const Item &it, int warp, int k) {
-    const int c = warp + kWarps * k;
-    const int tok = it.tok_begin + c * kChunk;
-    const int phys = p.block_tables[(long long)it.seq * p.max_blocks_per_seq + tok / p.block_size];
-    if (phys < 0 || phys >= p.num_blocks) {
-        flag_status(p.status, PA_STATUS_BAD_BLOCK_ID);
-        return -1;
-    }
-    return static_cast<int>(((long long)phys * p.num_kv_heads + it.kvh) * p.block_size +
-                            tok % p.block_size);
-}
-
-// The new token of a fused cache write, as one item sees it: the item's chunk
-// that holds position n - 1 (or -1), the row inside that chunk, and the row of
-// the [num_blocks * Hkv * block_size, head_dim] cache view to write.  Only the
-// last partition holds the new token; a slot that is not the slot of position
-// n - 1 is flagged once (KV head 0, head tile 0) and ignored.
-struct NewToken {
-    int chunk, row;
-    long long cache_row;
-};
-
-__device__ __forceinline__ NewToken new_token(const DecodeParams &p, const Item &it) {
-    NewToken t{-1, 0, -1};
-    if (!p.k_new || it.n <= 0 || it.tok_end != it.n) return t;
-    const int64_t slot = p.slot_mapping[it.seq];
-    if (slot < 0) return t;
-    const int pos = it.n - 1;
-    const int phys = p.block_tables[(long long)it.seq * p.max_blocks_per_seq + pos / p.block_size];
-    if (phys < 0 || phys >= p.num_blocks || slot != (int64_t)phys * p.block_size + pos % p.block_size) {
-        if (threadIdx.x == 0 && it.kvh == 0 && it.ht == 0) flag_status(p.status, PA_STATUS_BAD_SLOT);
-        return t;
-    }
-    t.chunk = (pos - it.tok_begin) / kChunk;
-    t.row = (pos - it.tok_begin) % kChunk;
-    t.cache_row = ((long long)phys * p.num_kv_heads + it.kvh) * p.block_size + pos % p.block_size;
-    return t;
-}
-
-// Work counter of the partition pass (one 64-bit word): hand-outs in the low
-// half, finished CTAs in the high half.  Every CTA makes all its hand-out
-// requests before it reports finishing, so when the last CTA reports, no
-// request is left and the word can go back to zero for the next launch.
-__device__ __forceinline__ long long next_handout(unsigned long long *ctr) {
-    return static_cast<long long>(atomicAdd(ctr, 1ull) & 0xffffffffull);
-}
-
-__device__ __forceinline__ void finish_handouts(unsigned long long *ctr) {
-    const unsigned long long before = atomicAdd(ctr, 1ull << 32);
-    if ((before >> 32) == gridDim.x - 1u) atomicExch(ctr, 0ull);
-}
 
 // ------------------------------------------------------------ bf16 path ---
 // Launch shape per head_dim: ring depth per warp and the CTAs per SM the
@@ -553,200 +364,6 @@ __global__ void __launch_bounds__(kWarps * 32, bf16_ctas_per_sm<HD>())
     }
 }
 
-// ------------------------------------------------------------ SIMT path ---
-// fp32 inputs, and bf16 inputs when the caller asks for it: plain fp32 FMAs,
-// one lane per head_dim slice, p kept in fp32.  Elements are widened to fp32 as
-// they are read from the staged tiles.
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// VEC consecutive elements of one staged row, widened to fp32.
-template <int VEC>
-__device__ __forceinline__ void load_row(const float *src, float (&dst)[VEC]) {
-    if constexpr (VEC == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src);
-        dst[0] = v.x, dst[1] = v.y, dst[2] = v.z, dst[3] = v.w;
-    } else {
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) dst[i] = src[i];
-    }
-}
-
-template <int VEC>
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *src, float (&dst)[VEC]) {
-    if constexpr (VEC == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(src);
-        __nv_bfloat162 a, b;
-        memcpy(&a, &raw.x, 4);
-        memcpy(&b, &raw.y, 4);
-        const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-        dst[0] = fa.x, dst[1] = fa.y, dst[2] = fb.x, dst[3] = fb.y;
-    } else {
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) dst[i] = __bfloat162float(src[i]);
-    }
-}
-
-template <typename T, int HD, int NSTAGE>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_simt_kernel(const DecodeParams p) {
-    constexpr int VEC = HD / 32;                 // head_dim elements per lane
-    constexpr int HT = 8;                        // query heads per tile
-    constexpr int PAGE_BYTES = kChunk * HD * static_cast<int>(sizeof(T));
-    constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
-    constexpr int WARP_BYTES = NSTAGE * STAGE_BYTES;
-    constexpr int LD = HD + kEpiPad;
-    static_assert(WARP_BYTES >= (16 * LD + 32) * 4, "epilogue tile must fit in a warp's stages");
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align_1024(smem_raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *wbuf = smem + warp * WARP_BYTES;
-    const uint32_t wbuf_s = smem_addr(wbuf);
-    const uint32_t bar_s = smem_addr(smem + kWarps * WARP_BYTES) + warp * NSTAGE * 8;
-    if (lane == 0) {
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(bar_s + 8 * s, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    uint32_t n_issued = 0, n_done = 0;
-    bool failed = false;
-    SeqCursor cur{0, 0};
-    const char *kc = static_cast<const char *>(p.k_cache);
-    const char *vc = static_cast<const char *>(p.v_cache);
-
-    for (long long item = blockIdx.x;; item += gridDim.x) {
-        Item it;
-        if (!next_item(it, cur, item, p, HT, lane)) break;
-        const int my_n = it.nchunks > warp ? (it.nchunks - warp + kWarps - 1) / kWarps : 0;
-        int rowA = -1, rowB = -1;
-        if (lane < my_n) rowA = chunk_row(p, it, warp, lane);
-        if (lane + 32 < my_n) rowB = chunk_row(p, it, warp, lane + 32);
-
-        auto issue = [&](int k) {
-            const int row = __shfl_sync(kFull, k < 32 ? rowA : rowB, k & 31);
-            if (failed) return;
-            if (lane == 0) {
-                const int s = n_issued % NSTAGE;
-                const uint32_t dst = wbuf_s + s * STAGE_BYTES, bar = bar_s + 8 * s;
-                fence_proxy_async_smem();
-                // An invalid block id completes the stage with no data (flagged).
-                mbar_arrive_expect_tx(bar, row >= 0 ? STAGE_BYTES : 0);
-                if (row >= 0) {
-                    const long long off = (long long)row * HD * static_cast<long long>(sizeof(T));
-                    bulk_load(dst, kc + off, PAGE_BYTES, bar);
-                    bulk_load(dst + PAGE_BYTES, vc + off, PAGE_BYTES, bar);
-                }
-            }
-            ++n_issued;
-        };
-
-        float q[HT][VEC];
-        {
-            const T *qb = static_cast<const T *>(p.q) +
-                          ((long long)it.seq * p.num_q_heads + it.qh0) * HD + lane * VEC;
-#pragma unroll
-            for (int h = 0; h < HT; ++h)
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) q[h][v] = h < it.rows ? to_f32(qb[h * HD + v]) : 0.f;
-        }
-        const int pro = my_n < NSTAGE ? my_n : NSTAGE;
-        for (int k = 0; k < pro; ++k) issue(k);
-        const NewToken ntok = new_token(p, it);
-
-        float acc[HT][VEC], m[HT], l[HT];
-#pragma unroll
-        for (int h = 0; h < HT; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[h][v] = 0.f;
-        }
-
-        for (int k = 0; k < my_n; ++k) {
-            const int s = n_done % NSTAGE;
-            const uint32_t parity = (n_done / NSTAGE) & 1u;
-            bool ok = !failed && mbar_wait_bounded(bar_s + 8 * s, parity);
-            if (__any_sync(kFull, !ok)) {
-                if (!failed && lane == 0) flag_status(p.status, PA_STATUS_WAIT_TIMEOUT);
-                failed = true;
-                break;
-            }
-            ++n_done;
-            const T *Ks = reinterpret_cast<const T *>(wbuf + s * STAGE_BYTES);
-            const T *Vs = Ks + kChunk * HD;
-            const int tok0 = it.tok_begin + (warp + kWarps * k) * kChunk;
-            const int valid = min(kChunk, it.tok_end - tok0);
-            if (warp + kWarps * k == ntok.chunk) {
-                // Fused cache write (see the bf16 kernel); plain row layout here.
-                constexpr int V16 = HD * static_cast<int>(sizeof(T)) / 16;   // 16-byte pieces per row
-                const long long src = ((long long)it.seq * p.num_kv_heads + it.kvh) * V16;
-                const uint4 *kn = static_cast<const uint4 *>(p.k_new) + src;
-                const uint4 *vn = static_cast<const uint4 *>(p.v_new) + src;
-                uint4 *st = reinterpret_cast<uint4 *>(wbuf + s * STAGE_BYTES);
-                for (int i = lane; i < 2 * V16; i += 32) {
-                    const bool isv = i >= V16;
-                    const int c = isv ? i - V16 : i;
-                    const uint4 val = isv ? vn[c] : kn[c];
-                    st[(isv ? kChunk * V16 : 0) + ntok.row * V16 + c] = val;
-                    if (it.ht == 0)
-                        static_cast<uint4 *>(isv ? p.v_cache_w : p.k_cache_w)[ntok.cache_row * V16 + c] = val;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            for (int tt = 0; tt < valid; ++tt) {
-                float kv[VEC], vv[VEC];
-                load_row<VEC>(Ks + tt * HD + lane * VEC, kv);
-                load_row<VEC>(Vs + tt * HD + lane * VEC, vv);
-#pragma unroll
-                for (int h = 0; h < HT; ++h) {
-                    if (h < it.rows) {
-                        float d = 0.f;
-#pragma unroll
-                        for (int v = 0; v < VEC; ++v) d = fmaf(q[h][v], kv[v], d);
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
-                        const float sv = d * p.scale_log2;
-                        const float mn = fmaxf(m[h], sv);
-                        const float a = exp2f(m[h] - mn);
-                        const float pr = exp2f(sv - mn);
-                        l[h] = l[h] * a + pr;
-#pragma unroll
-                        for (int v = 0; v < VEC; ++v) acc[h][v] = fmaf(acc[h][v], a, pr * vv[v]);
-                        m[h] = mn;
-                    }
-                }
-            }
-            __syncwarp();
-            if (k + NSTAGE < my_n) issue(k + NSTAGE);
-        }
-
-        {
-            float *eo = reinterpret_cast<float *>(wbuf);
-#pragma unroll
-            for (int h = 0; h < HT; ++h)
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) eo[h * LD + lane * VEC + v] = acc[h][v];
-            if (lane == 0) {
-#pragma unroll
-                for (int h = 0; h < 16; ++h) {
-                    eo[16 * LD + h] = h < HT ? m[h < HT ? h : 0] : -INFINITY;
-                    eo[16 * LD + 16 + h] = h < HT ? l[h < HT ? h : 0] : 0.f;
-                }
-            }
-        }
-        __syncthreads();
-        merge_and_store<T, HD>(smem, WARP_BYTES, p, it.seq, it.part, it.qh0, it.rows, it.single);
-        fence_proxy_async_smem();
-        __syncthreads();
-    }
-    if (failed && lane == 0) {
-        for (uint32_t gi = n_done; gi < n_issued; ++gi)
-            mbar_wait_bounded(bar_s + 8 * (gi % NSTAGE), (gi / NSTAGE) & 1u);
-    }
-}
-
 // ------------------------------------------------------- split-K reduce ---
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p, for
 // every (sequence, query head) whose context spans more than one partition.
@@ -828,91 +445,7 @@ namespace {
 
 using pa::DecodeParams;
 
-constexpr int kMaxDevices = 64;
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-long long l2_bytes(int dev) {
-    static std::atomic<long long> cache[kMaxDevices];
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    long long b = cache[dev].load(std::memory_order_relaxed);
-    if (b == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
-        b = v;
-        cache[dev].store(b, std::memory_order_relaxed);
-    }
-    return b;
-}
-
-int sm_count(int dev) {
-    static std::atomic<int> cache[kMaxDevices];
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    int n = cache[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
-}
-
-// Per-kernel launch facts: dynamic smem set once, occupancy cached per device
-// (guarded, so concurrent first calls from several host threads are safe).
-struct KernelSlot {
-    int smem = 0;
-    int occupancy[kMaxDevices] = {0};
-    std::mutex mu;
-};
-
-template <typename K>
-int ensure_kernel(K kernel, KernelSlot &slot, int smem, int dev) {
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    std::lock_guard<std::mutex> lock(slot.mu);
-    if (slot.occupancy[dev] == 0) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return 0;
-        int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, pa::kWarps * 32, smem) != cudaSuccess ||
-            occ <= 0)
-            return 0;
-        slot.smem = smem;
-        slot.occupancy[dev] = occ;
-    }
-    return slot.occupancy[dev];
-}
-
-bool make_map(CUtensorMap *map, const void *base, long long rows, int hd) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(hd) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pa::kChunk)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-template <typename T>
-constexpr int simt_stages() { return sizeof(T) == 4 ? 2 : 3; }
+using namespace pa::host;
 
 template <int HD, bool ROWS16>
 int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache, long long items,
@@ -930,20 +463,6 @@ int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache,
     const long long cap = static_cast<long long>(sm_count(dev)) * occ;
     const int grid = static_cast<int>(items < cap ? items : cap);
     kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(mk, mv, p);
-    return PA_OK;
-}
-
-template <typename T, int HD>
-int launch_simt(const DecodeParams &p, long long items, int dev, cudaStream_t st) {
-    constexpr int NS = simt_stages<T>();
-    constexpr int SMEM = pa::kWarps * NS * 2 * pa::kChunk * HD * static_cast<int>(sizeof(T)) + pa::kWarps * NS * 8 + 1024;
-    static KernelSlot slot;
-    auto kernel = pa::decode_simt_kernel<T, HD, NS>;
-    const int occ = ensure_kernel(kernel, slot, SMEM, dev);
-    if (occ == 0) return pa_fail(PA_ERR_CUDA, "pa_decode: cannot configure the SIMT kernel");
-    const long long cap = static_cast<long long>(sm_count(dev)) * occ;
-    const int grid = static_cast<int>(items < cap ? items : cap);
-    kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(p);
     return PA_OK;
 }
 
@@ -1103,25 +622,21 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     int rc = PA_OK;
     if (a->phase == PA_PHASE_REDUCE) {
         // only the merge pass below
-    } else if (use_mma) {
-        const bool rows16 = p.group > 8;
+    } else {
         if (p.work_ctr && !a->skip_counter_reset &&
             cudaMemsetAsync(p.work_ctr, 0, sizeof(unsigned long long), st) != cudaSuccess)
             return pa_fail(PA_ERR_CUDA, "pa_decode: cannot reset the work counter");
-        if (head_dim == 128)
-            rc = rows16 ? launch_bf16<128, true>(p, k_cache, v_cache, items, dev, st)
-                        : launch_bf16<128, false>(p, k_cache, v_cache, items, dev, st);
-        else
-            rc = rows16 ? launch_bf16<64, true>(p, k_cache, v_cache, items, dev, st)
-                        : launch_bf16<64, false>(p, k_cache, v_cache, items, dev, st);
-    } else {
-        p.work_ctr = nullptr;   // the SIMT kernel walks its items statically
-        if (a->dtype == PA_BF16)
-            rc = head_dim == 128 ? launch_simt<__nv_bfloat16, 128>(p, items, dev, st)
-                                 : launch_simt<__nv_bfloat16, 64>(p, items, dev, st);
-        else
-            rc = head_dim == 128 ? launch_simt<float, 128>(p, items, dev, st)
-                                 : launch_simt<float, 64>(p, items, dev, st);
+        if (use_mma) {
+            const bool rows16 = p.group > 8;
+            if (head_dim == 128)
+                rc = rows16 ? launch_bf16<128, true>(p, k_cache, v_cache, items, dev, st)
+                            : launch_bf16<128, false>(p, k_cache, v_cache, items, dev, st);
+            else
+                rc = rows16 ? launch_bf16<64, true>(p, k_cache, v_cache, items, dev, st)
+                            : launch_bf16<64, false>(p, k_cache, v_cache, items, dev, st);
+        } else {
+            rc = pa::launch_simt_pass(p, k_cache, v_cache, a->dtype == PA_F32, head_dim, items, dev, st);
+        }
     }
     if (rc != PA_OK) return rc;
     if (max_parts > 1 && a->phase != PA_PHASE_PARTITIONS) {

@@ -40,7 +40,7 @@ def test_traffic_figure_is_withheld_once_the_code_changes(tmp_path, monkeypatch)
     src = os.path.join(bench.ROOT, "paged_kv_cache_237_gb300", "csrc")
     fake = tmp_path / "paged_kv_cache_237_gb300" / "csrc"
     fake.mkdir(parents=True)
-    for name in ("pa_decode.cu", "pa_internal.h"):
+    for name in bench.KERNEL_FILES:
         shutil.copy(os.path.join(src, name), fake / name)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     have = bench.captured_traffic("long_context")

@@ -56,6 +56,30 @@ def test_bf16_workload_step_full_parity(pa, name, kw):
     assert_decode_close(out, ref, torch.bfloat16, what=name)
 
 
+@pytest.mark.parametrize("name", ["mha_llama2_7b_f32", "gqa_llama3_70b_f32"])
+def test_f32_workload_step_full_parity(pa, name):
+    """The MHA and GQA batches in fp32 (the fp32-FMA pass): every output within
+    1e-5 of the oracle, the cache write bit-exact, and the fused write (the
+    launch the benchmark times) bit-identical to write-then-decode."""
+    binding, engine, workloads = pa
+    d, step, out, kc0, vc0 = step_and_check(pa, name)
+    oracle.reshape_and_cache(d["k_new"].cpu(), d["v_new"].cpu(), kc0, vc0, d["slot_mapping"].cpu())
+    assert torch.equal(bits(d["k_cache"].cpu()), bits(kc0))
+    assert torch.equal(bits(d["v_cache"].cpu()), bits(vc0))
+    ref = oracle_decode(d["q"], kc0, vc0, d["block_tables"], d["context_lens"], d["scale"])
+    assert_decode_close(out, ref, torch.float32, what=name)
+    first = out.clone()
+    d2 = workloads.decode_inputs(name, device="cuda")
+    w = d2["workload"]
+    step2 = engine.DecodeStep(d2["q"], d2["k_cache"], d2["v_cache"], d2["block_tables"], d2["context_lens"],
+                              d2["scale"], d2["max_context_len"], w.partition_size)
+    fused = step2.run_fused(d2["k_new"], d2["v_new"], d2["slot_mapping"])
+    torch.cuda.synchronize()
+    assert step2.status.read() == 0
+    assert torch.equal(bits(fused), bits(first))
+    assert torch.equal(bits(d2["k_cache"]), bits(d["k_cache"]))
+
+
 def test_prefix_share_step_with_copy_on_write(pa):
     binding, engine, _ = pa
     st = engine.prefix_share_state("cuda")
