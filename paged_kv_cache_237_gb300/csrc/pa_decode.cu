@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(kWarps * 32, bf16_ctas_per_sm<HD>())
     SeqCursor cur{0, 0};
     const int oob_row = p.total_rows;
     const uint64_t kv_policy = l2_evict_first_policy();
+    // Launched as a programmatic dependent: everything above touched only this
+    // CTA's registers and shared memory; from here on it reads what earlier
+    // work in the stream wrote (q, tables, caches, the work counter).
+    griddep_wait();
 
     // Work items: a CTA's first is blockIdx.x; later ones come from the work
     // counter in the workspace when there is one (a CTA that finishes early
@@ -370,10 +374,11 @@ __global__ void __launch_bounds__(kWarps * 32, bf16_ctas_per_sm<HD>())
 // One CTA per (query head, sequence): the threads first take M over all
 // partitions, then each warp sums a strided subset of the partitions (lanes own
 // 4 consecutive head_dim values) and the warps' sums are added in shared memory.
-constexpr int kReduceWarps = 8;
-
-template <typename OutT, int HD>
+template <typename OutT, int HD, int kReduceWarps>
 __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
+    // A following pass may be scheduled as soon as every merge CTA is running
+    // (it waits for this grid before reading anything).
+    griddep_launch_dependents();
     griddep_wait();   // the partition pass (launched before, programmatically) is done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qh = blockIdx.x;
@@ -462,7 +467,8 @@ int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache,
         return pa_fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed");
     const long long cap = static_cast<long long>(sm_count(dev)) * occ;
     const int grid = static_cast<int>(items < cap ? items : cap);
-    kernel<<<grid, pa::kWarps * 32, SMEM, st>>>(mk, mv, p);
+    const cudaError_t e = launch_dependent(kernel, grid, pa::kWarps * 32, SMEM, st, mk, mv, p);
+    if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
     return PA_OK;
 }
 
@@ -470,11 +476,17 @@ int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache,
 // CTAs may become resident while the pass's last CTAs finish, and wait in
 // griddep_wait() until the pass is complete.  After any other kind of
 // predecessor it simply starts when that one has finished.
+// Warps per merge CTA: 4 while no sequence has more than 64 partitions (up to
+// 16 CTAs per SM, so a batch's (head, sequence) rows fit in one wave), else 8
+// (long sequences spread their partitions over more warps).
+constexpr int kReduceMaxPartsSmall = 64;
+
 template <typename OutT, int HD>
 cudaError_t launch_reduce(const DecodeParams &p, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
+    const bool small = p.max_parts <= kReduceMaxPartsSmall;
     cfg.gridDim = dim3(p.num_q_heads, p.num_seqs);
-    cfg.blockDim = dim3(pa::kReduceWarps * 32);
+    cfg.blockDim = dim3((small ? 4 : 8) * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -482,7 +494,8 @@ cudaError_t launch_reduce(const DecodeParams &p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pa::decode_reduce_kernel<OutT, HD>, p);
+    return small ? cudaLaunchKernelEx(&cfg, pa::decode_reduce_kernel<OutT, HD, 4>, p)
+                 : cudaLaunchKernelEx(&cfg, pa::decode_reduce_kernel<OutT, HD, 8>, p);
 }
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }

@@ -161,6 +161,9 @@ __global__ void __launch_bounds__(NW * 32, CPS)
     const uint64_t kv_policy = l2_evict_first_policy();
     const int tok = lane & 15, half = lane >> 4;      // q.K roles
     const int dg = lane % GPR, ts = lane / GPR;       // p.V roles
+    // Launched as a programmatic dependent: from here on the CTA reads what
+    // earlier work in the stream wrote (q, tables, caches, the work counter).
+    griddep_wait();
 
     // Work items as in the tensor-core pass: the first is blockIdx.x, later
     // ones come from the work counter (one fetched ahead) when there is one,
@@ -444,7 +447,8 @@ int launch_one(const DecodeParams &p, const void *k_cache, const void *v_cache, 
         return pa_fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed");
     const long long cap = static_cast<long long>(host::sm_count(dev)) * occ;
     const int grid = static_cast<int>(items < cap ? items : cap);
-    kernel<<<grid, S::NW * 32, Lay::SMEM, st>>>(mk, mv, p);
+    const cudaError_t e = host::launch_dependent(kernel, grid, S::NW * 32, Lay::SMEM, st, mk, mv, p);
+    if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, cudaGetErrorString(e));
     return PA_OK;
 }
 
