@@ -45,10 +45,11 @@ L2_BYTES = 129 * 2**20
 # seeded slice of the same length mix (--num-seqs), scaled to the full launch
 # by the ratio of algorithmic bytes.  Valid only while the kernel source is
 # the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "cc4cbf6d384692de",
-                   # 48-sequence slice: 4,143,344,640 B read + 26,897,920 B written
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "5335d2888b5406e7",
+                   # 48-sequence slice: 4,143,341,056 B read + 27,327,488 B written
                    # over 4,141,526,704 algorithmic bytes, scaled to 20,791,665,640
-                   "bytes_per_launch": {"long_context": 20935827568}}
+                   "bytes_per_launch": {"long_context": 20937966132,
+                                        "gqa_llama3_70b": 902336512 + 6594560}}
 
 
 KERNEL_FILES = ("pa_decode.cu", "pa_decode_common.cuh", "pa_internal.h")
