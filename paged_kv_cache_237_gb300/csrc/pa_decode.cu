@@ -591,8 +591,6 @@ extern "C" int pa_decode(void *out, const void *q, const void *k_cache, const vo
     }
     p.out = out;
     p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.status = a->dev_status;

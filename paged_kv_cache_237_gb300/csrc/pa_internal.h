@@ -36,8 +36,6 @@ constexpr unsigned kFull = 0xffffffffu;
 struct DecodeParams {
     void *out;
     const void *q;
-    const void *k_cache;   // used by the fp32 path (1-D bulk copies)
-    const void *v_cache;
     const int32_t *block_tables;
     const int32_t *context_lens;
     float *part_ml;        // [S][max_parts][Hq][2]  (running max in log2 units, sum)
@@ -140,16 +138,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Untiled bulk copy global -> shared (16-byte aligned, size multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

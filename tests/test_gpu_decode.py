@@ -32,7 +32,7 @@ def run(pa, q, kc, vc, tables, lens, scale, partition_size=0, status=None, max_c
 @pytest.mark.parametrize("dtype,simt", [(torch.bfloat16, False), (torch.bfloat16, True), (torch.float32, False)])
 @pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("bs", [16, 32])
-@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (16, 2), (16, 1), (12, 4), (40, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (6, 3), (8, 2), (16, 2), (16, 1), (12, 4), (40, 2)])
 def test_edge_lengths_match_oracle(pa, dtype, simt, hd, bs, Hq, Hkv):
     q, kc, vc, tables, lens = make_case(EDGE_LENS, Hq, Hkv, hd, bs, dtype, seed=hd + bs + Hq)
     scale = 1.0 / math.sqrt(hd)

@@ -21,8 +21,12 @@ def pa():
     return binding
 
 
-def draw(rng):
+def draw(rng, fma_pass=False):
+    """One configuration; fma_pass draws only cases of the fp32-FMA pass (fp32
+    inputs, or bf16 with simt)."""
     dtype = torch.bfloat16 if rng.random() < 0.75 else torch.float32
+    if fma_pass:
+        dtype = torch.float32 if rng.random() < 0.7 else torch.bfloat16
     hd = int(rng.choice([64, 128]))
     bs = int(rng.choice([16, 32]))
     Hkv = int(rng.choice([1, 2, 4, 8]))
@@ -39,14 +43,24 @@ def draw(rng):
         else:
             lens.append(int(rng.integers(1, 3000)))
     fused = bool(rng.random() < 0.5)
-    simt = dtype == torch.bfloat16 and bool(rng.random() < 0.3)
+    simt = dtype == torch.bfloat16 and (fma_pass or bool(rng.random() < 0.3))
     return dtype, hd, bs, Hkv, group * Hkv, P, lens, fused, simt
 
 
 @pytest.mark.parametrize("seed", range(40))
 def test_random_configuration_matches_oracle(pa, seed):
-    rng = np.random.default_rng(1000 + seed)
-    dtype, hd, bs, Hkv, Hq, P, lens, fused, simt = draw(rng)
+    check_random_case(pa, seed, np.random.default_rng(1000 + seed), fma_pass=False)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_fma_pass_configuration_matches_oracle(pa, seed):
+    """The same sweep restricted to the fp32-FMA pass (head tiles of 1, 2, 4
+    and 8 query heads, both head_dims, packed-FMA products)."""
+    check_random_case(pa, 500 + seed, np.random.default_rng(5000 + seed), fma_pass=True)
+
+
+def check_random_case(pa, seed, rng, fma_pass):
+    dtype, hd, bs, Hkv, Hq, P, lens, fused, simt = draw(rng, fma_pass)
     q, kc, vc, tables, lens_t = make_case(lens, Hq, Hkv, hd, bs, dtype, seed=seed, slack=int(rng.integers(0, 9)))
     scale = float(rng.uniform(0.02, 0.2)) if rng.random() < 0.9 else 1.0 / math.sqrt(hd)
     max_ctx = max(lens) if max(lens) > 0 else 1
