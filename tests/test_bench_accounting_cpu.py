@@ -52,3 +52,9 @@ def test_traffic_figure_is_withheld_once_the_code_changes(tmp_path, monkeypatch)
         f.write("static int an_edit = 1;\n")
     assert bench.captured_traffic("long_context") is None
     assert bench.captured_traffic("no_such_workload") is None
+
+
+def test_bandwidth_fractions_name_their_denominators():
+    f = bench.fractions(6787.6, 6787.6)
+    assert f == {"of_measured_copy_peak": 1.0, "of_datasheet_7900_GBps": round(6787.6 / 7900.0, 4)}
+    assert bench.fractions(3393.8, 6787.6)["of_measured_copy_peak"] == 0.5

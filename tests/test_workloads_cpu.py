@@ -82,3 +82,31 @@ def test_generators_are_deterministic():
     # chunked drawing equals one draw of the same stream
     assert torch.equal(randn((4, 100), torch.float32, 9, "cpu", chunk_elems=64),
                        randn((4, 100), torch.float32, 9, "cpu"))
+
+
+def test_a_slice_keeps_the_first_sequences_of_the_drawn_batch():
+    """num_seqs keeps the first sequences of the same draw (lengths in their
+    seeded order), with the pool sized by the workload's own rule."""
+    from paged_kv_cache_237_gb300.workloads import decode_inputs
+    w, full = lengths("gqa_llama3_70b")
+    d = decode_inputs("gqa_llama3_70b", device="cpu", num_seqs=3)
+    assert d["lens"].tolist() == full[:3].tolist()
+    need = sum(-(-int(n) // w.block_size) for n in full[:3])
+    assert d["num_blocks"] == pool_blocks(w, need) and d["k_cache"].shape[0] == d["num_blocks"]
+    assert d["q"].shape == (3, w.num_q_heads, w.head_dim) and d["block_tables"].shape[0] == 3
+
+
+@pytest.mark.parametrize("name", ["mha_llama2_7b", "gqa_llama3_70b"])
+def test_fp32_twins_share_lengths_placement_and_values(name):
+    """The fp32 batches draw the same lengths, placement and N(0, 1) values as
+    their bf16 counterparts; the bf16 values are the fp32 ones rounded."""
+    import torch
+    from paged_kv_cache_237_gb300.workloads import decode_inputs
+    a = decode_inputs(name, device="cpu", num_seqs=2)
+    b = decode_inputs(name + "_f32", device="cpu", num_seqs=2)
+    assert b["workload"].dtype == torch.float32 and a["workload"].dtype == torch.bfloat16
+    assert a["lens"].tolist() == b["lens"].tolist()
+    assert np.array_equal(a["tables"], b["tables"]) and a["num_blocks"] == b["num_blocks"]
+    for key in ("q", "k_cache", "v_cache", "k_new", "v_new"):
+        assert torch.equal(b[key].to(torch.bfloat16), a[key]), key
+    assert torch.equal(a["slot_mapping"], b["slot_mapping"])
