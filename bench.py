@@ -338,8 +338,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the same-run measurements of the other workloads, the placement study and "
-                         "the cache-op sizes")
+                    help="skip the same-run measurements of the other workloads and of the placement, cache-op, "
+                         "prefix-cache and swap studies")
     ap.add_argument("--simt", action="store_true",
                     help="bf16 products on plain fp32 FMAs (SIMT kernel) instead of tensor-core MMAs")
     ap.add_argument("--unfused", action="store_true",
@@ -612,7 +612,7 @@ def main():
                "single_core_value": round(sample_kv_bytes(d, one) / dt1 / 1e9, 4),
                "single_core_sample": f"{len(one)} sequences, 1 thread, {dt1:.1f} s"}
 
-    secondary = placement = cache_ops = None
+    secondary = placement = cache_ops = prefix_cache = swap = None
     peak, peak_src = load_peak()
     if rank == 0 and world == 1 and args.workload == "long_context" and args.num_seqs is None \
             and not args.no_secondary:
@@ -630,6 +630,9 @@ def main():
         placement = placement_block("long_context", 40, args.warmup)
         # cache write and block copy at a decode step's size and at streaming sizes
         cache_ops = cache_ops_block(100, args.warmup, tokens=(256, 65536), pairs=(24, 2048))
+        # prefix caching over a multi-tenant batch, and block swaps to pinned host memory
+        prefix_cache = prefix_cache_block(100, args.warmup)
+        swap = swap_block(20, args.warmup)
 
     if rank != 0:
         if dist is not None:
@@ -695,6 +698,10 @@ def main():
         line["placement"] = placement
     if cache_ops is not None:
         line["cache_ops"] = cache_ops
+    if prefix_cache is not None:
+        line["prefix_cache"] = prefix_cache
+    if swap is not None:
+        line["swap"] = swap
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -757,18 +764,23 @@ def run_placement_study(args):
           flush=True)
 
 
-def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_len: int = 2048):
+def run_prefix_cache_study(args):
+    from paged_kv_cache_237_gb300 import build as pa_build
+    pa_build.build()
+    torch.cuda.set_device(0)
+    print(json.dumps({"study": "prefix_cache", **prefix_cache_block(args.steps, args.warmup)}), flush=True)
+
+
+def prefix_cache_block(steps: int, warmup: int, tenants: int = 4, per_tenant: int = 64,
+                       prompt_len: int = 2048) -> dict:
     """A multi-tenant batch admitted through the chained-key prefix cache: each
     tenant has its own 2048-token system prompt (salted by tenant), each
     request adds a private question of 16..512 tokens.  Reports host admission
     cost, blocks held with and without sharing, and the decode step over the
     shared blocks (GQA 64/8, head_dim 128, bs 16, bf16)."""
-    from paged_kv_cache_237_gb300 import build as pa_build
-    pa_build.build()
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.engine import DecodeStep
     from paged_kv_cache_237_gb300.workloads import randn
-    torch.cuda.set_device(0)
     rng = np.random.default_rng(7)
     bs, Hq, Hkv, hd = 16, 64, 8, 128
     systems = [rng.integers(0, 128000, size=prompt_len).tolist() for _ in range(tenants)]
@@ -790,7 +802,7 @@ def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_
     held = bm.num_blocks - bm.num_free()
     max_blocks = max(len(bm.block_table(s)) for s in seqs)
     tables, lens = bm.build_tables(seqs, max_blocks)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     nb = bm.num_blocks
     q = randn((len(seqs), Hq, hd), torch.bfloat16, 71, dev)
     kc = randn((nb, Hkv, bs, hd), torch.bfloat16, 72, dev)
@@ -800,10 +812,10 @@ def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_
     step = DecodeStep(q, kc, vc, tables.to(dev), lens.to(dev), 1 / math.sqrt(hd), int(lens.max()))
     sl = slots.to(dev)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step.run_fused(kn, vn, sl, stream=stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         a.record(stream)
         step.run_fused(kn, vn, sl, stream=stream)
@@ -814,28 +826,36 @@ def run_prefix_cache_study(args, tenants: int = 4, per_tenant: int = 64, prompt_
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     logical = decode_bytes(lens.tolist(), Hq, Hkv, hd, bs, 2, 2, 2)
     unique_kv = held * Hkv * bs * hd * 2 * 2
-    print(json.dumps({
-        "study": "prefix_cache", "tenants": tenants, "requests": len(reqs), "system_prompt_tokens": prompt_len,
+    bm.close()
+    del q, kc, vc, kn, vn, step
+    torch.cuda.empty_cache()
+    return {
+        "tenants": tenants, "requests": len(reqs), "system_prompt_tokens": prompt_len,
         "copy_on_write_pairs": int(pairs.shape[0]),
         "host_admission_us_per_request": round(admit_s / len(reqs) * 1e6, 2),
         "cached_tokens_at_admission": int(cached_tokens),
         "blocks_held": int(held), "blocks_without_sharing": int(unshared),
         "memory_saved": round(1 - held / unshared, 4),
         "decode_step_ms": round(ms, 4), "logical_kv_GBps": round(logical / (ms * 1e-3) / 1e9, 1),
-        "unique_kv_bytes": int(unique_kv), "unique_kv_GBps": round(unique_kv / (ms * 1e-3) / 1e9, 1)}),
-        flush=True)
+        "unique_kv_bytes": int(unique_kv), "unique_kv_GBps": round(unique_kv / (ms * 1e-3) / 1e9, 1),
+        "timing": "eager decode steps (fused write), events around each"}
 
 
-def run_swap_study(args, num_blocks: int = 4096):
-    """Swap-out (device -> pinned host) and swap-in (host -> device) of
-    `num_blocks` scattered blocks of the long-context geometry (8 KV heads,
-    block_size 32, head_dim 128, bf16: 128 KB of K+V per block)."""
+def run_swap_study(args):
     from paged_kv_cache_237_gb300 import build as pa_build
     pa_build.build()
+    torch.cuda.set_device(0)
+    print(json.dumps({"study": "swap", **swap_block(args.steps, args.warmup)}), flush=True)
+
+
+def swap_block(steps: int, warmup: int, num_blocks: int = 4096) -> dict:
+    """Swap-out (device -> pinned host) and swap-in (host -> device) of
+    `num_blocks` scattered blocks of the long-context geometry (8 KV heads,
+    block_size 32, head_dim 128, bf16: 128 KB of K+V per block), and the copy
+    engines on one contiguous range of the same size for comparison."""
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.workloads import randn
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     Hkv, bs, hd = 8, 32, 128
     pool = 3 * num_blocks
     dk = randn((pool, Hkv, bs, hd), torch.bfloat16, 81, dev)
@@ -852,10 +872,10 @@ def run_swap_study(args, num_blocks: int = 4096):
     nbytes = num_blocks * Hkv * bs * hd * 2 * 2
 
     def timed(fn):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in ev:
             a.record(stream)
             fn()
@@ -880,12 +900,13 @@ def run_swap_study(args, num_blocks: int = 4096):
         dflat_k.copy_(hflat_k, non_blocking=True)
         dflat_v.copy_(hflat_v, non_blocking=True)
     mc_out, mc_in = timed(memcpy_out), timed(memcpy_in)
-    print(json.dumps({"study": "swap", "blocks": num_blocks, "bytes_each_way": nbytes,
-                      "swap_out_ms": round(ms_out, 4), "swap_out_GBps": round(nbytes / (ms_out * 1e-3) / 1e9, 1),
-                      "swap_in_ms": round(ms_in, 4), "swap_in_GBps": round(nbytes / (ms_in * 1e-3) / 1e9, 1),
-                      "contiguous_memcpy_out_GBps": round(nbytes / (mc_out * 1e-3) / 1e9, 1),
-                      "contiguous_memcpy_in_GBps": round(nbytes / (mc_in * 1e-3) / 1e9, 1)}),
-          flush=True)
+    del dk, dv, hk, hv
+    torch.cuda.empty_cache()
+    return {"blocks": num_blocks, "bytes_each_way": nbytes,
+            "swap_out_ms": round(ms_out, 4), "swap_out_GBps": round(nbytes / (ms_out * 1e-3) / 1e9, 1),
+            "swap_in_ms": round(ms_in, 4), "swap_in_GBps": round(nbytes / (ms_in * 1e-3) / 1e9, 1),
+            "contiguous_memcpy_out_GBps": round(nbytes / (mc_out * 1e-3) / 1e9, 1),
+            "contiguous_memcpy_in_GBps": round(nbytes / (mc_in * 1e-3) / 1e9, 1)}
 
 
 def cache_ops_block(steps: int, warmup: int, tokens=(256, 4096, 65536), pairs=(24, 256, 2048)) -> dict:
