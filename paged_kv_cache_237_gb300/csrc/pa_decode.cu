@@ -394,9 +394,31 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
     __shared__ float s_max[kReduceWarps];
     __shared__ float s_l[kReduceWarps];
     __shared__ float4 s_acc[kReduceWarps][HD / 4];
+    const bool active = lane < HD / 4;
+
+    // Staged variant (4-warp CTAs, at most kReduceMaxPartsSmall partitions):
+    // every partial of the row is copied into shared memory at once (cp.async,
+    // no registers held), so the row costs one round trip however many
+    // partitions it has.  Otherwise the partials are read as they are summed.
+    constexpr bool kStaged = kReduceWarps == 4;
+    extern __shared__ float4 s_stage[];            // [max_parts][HD / 4] accumulators, then [max_parts] (m, l)
+    float2 *s_ml = reinterpret_cast<float2 *>(s_stage + (kStaged ? p.max_parts * (HD / 4) : 0));
+    if constexpr (kStaged) {
+        if (active)
+            for (int i = warp; i < np; i += kReduceWarps)
+                cp_async_16(smem_addr(s_stage + i * (HD / 4) + lane), p.part_acc + (base + i * stride) * HD + lane * 4);
+        for (int i = threadIdx.x; i < np; i += blockDim.x)
+            cp_async_8(smem_addr(s_ml + i), p.part_ml + (base + i * stride) * 2);
+        cp_async_wait_all();
+        __syncthreads();
+    }
+    auto ml_of = [&](int i) -> float2 {
+        if constexpr (kStaged) return s_ml[i];
+        return *reinterpret_cast<const float2 *>(p.part_ml + (base + i * stride) * 2);
+    };
 
     float M = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += blockDim.x) M = fmaxf(M, p.part_ml[(base + i * stride) * 2]);
+    for (int i = threadIdx.x; i < np; i += blockDim.x) M = fmaxf(M, ml_of(i).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     if (lane == 0) s_max[warp] = M;
@@ -407,15 +429,17 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
 
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool active = lane < HD / 4;
 #pragma unroll 4
     for (int i = warp; i < np; i += kReduceWarps) {
-        const long long idx = base + i * stride;
-        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + idx * 2);
+        const float2 ml = ml_of(i);
         const float f = exp2f(ml.x - M);
         L += f * ml.y;
         if (active) {
-            const float4 v = *reinterpret_cast<const float4 *>(p.part_acc + idx * HD + lane * 4);
+            float4 v;
+            if constexpr (kStaged)
+                v = s_stage[i * (HD / 4) + lane];
+            else
+                v = *reinterpret_cast<const float4 *>(p.part_acc + (base + i * stride) * HD + lane * 4);
             acc.x += f * v.x;
             acc.y += f * v.y;
             acc.z += f * v.z;
@@ -476,9 +500,10 @@ int launch_bf16(const DecodeParams &p, const void *k_cache, const void *v_cache,
 // CTAs may become resident while the pass's last CTAs finish, and wait in
 // griddep_wait() until the pass is complete.  After any other kind of
 // predecessor it simply starts when that one has finished.
-// Warps per merge CTA: 4 while no sequence has more than 64 partitions (up to
-// 16 CTAs per SM, so a batch's (head, sequence) rows fit in one wave), else 8
-// (long sequences spread their partitions over more warps).
+// Warps per merge CTA: 4 while no sequence has more than 64 partitions -- a
+// row's partials are then staged in shared memory in one round trip (at most
+// 64 x (4 * head_dim + 8) bytes) -- else 8 (long sequences spread their
+// partitions over more warps, read as they are summed).
 constexpr int kReduceMaxPartsSmall = 64;
 
 template <typename OutT, int HD>
@@ -487,7 +512,7 @@ cudaError_t launch_reduce(const DecodeParams &p, cudaStream_t st) {
     const bool small = p.max_parts <= kReduceMaxPartsSmall;
     cfg.gridDim = dim3(p.num_q_heads, p.num_seqs);
     cfg.blockDim = dim3((small ? 4 : 8) * 32);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = small ? static_cast<size_t>(p.max_parts) * (HD * 4 + 8) : 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
