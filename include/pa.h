@@ -167,7 +167,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               float scale, const pa_decode_args *args);
 
 /* Bytes of workspace pa_decode needs for these sizes (0 when no sequence can
- * span more than one partition).  partition_size 0 means the default. */
+ * span more than one partition).  partition_size 0 means the default.  A
+ * helper of this library's split-K design: the pages describe no kernel-level
+ * split of long contexts, so this call has no counterpart there. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                 int max_context_len, int partition_size);
 
