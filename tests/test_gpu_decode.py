@@ -375,3 +375,56 @@ def test_loose_max_context_len_leaves_most_ctas_without_work(pa):
         assert status.read() == 0
         assert int(ws[:8].view(torch.int64).item()) == 0
         assert_decode_close(out, ref, torch.bfloat16, what=f"loose max_context_len, skip={skip}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_inputs_written_by_the_preceding_kernel_are_seen(pa, dtype):
+    """The partition pass is a programmatic dependent launch: it may be
+    scheduled while the kernel before it still runs, and must read nothing
+    before its grid-dependency wait.  Ordinary device kernels rewrite q, the
+    tables, the lengths and the caches right before each call (eagerly, then
+    inside a CUDA graph); every output must be the oracle's on the new inputs."""
+    from paged_kv_cache_237_gb300.engine import DecodeStep
+    Hq, Hkv, hd, bs = 16, 2, 128, 16
+    cases = [make_case(lens, Hq, Hkv, hd, bs, dtype, seed=60 + i, slack=3, nan_tails=False)
+             for i, lens in enumerate(([900, 33, 2100], [1500, 640, 17], [5, 2047, 1200]))]
+    nb = max(c[1].shape[0] for c in cases)
+    width = max(c[3].shape[1] for c in cases)
+    # one set of device buffers, large enough for every case
+    q = torch.zeros_like(cases[0][0])
+    kc = torch.zeros(nb, Hkv, bs, hd, dtype=dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    tables = torch.full((3, width), -1, dtype=torch.int32, device="cuda")
+    lens_t = torch.zeros(3, dtype=torch.int32, device="cuda")
+    step = DecodeStep(q, kc, vc, tables, lens_t, 1 / math.sqrt(hd), 2100, 256)
+
+    def load(case):
+        cq, ckc, cvc, ct, cl = case
+        q.copy_(cq)                      # device-to-device copy kernels, enqueued just before the call
+        kc[: ckc.shape[0]].copy_(ckc)
+        vc[: cvc.shape[0]].copy_(cvc)
+        tables.fill_(-1)
+        tables[:, : ct.shape[1]].copy_(ct)
+        lens_t.copy_(cl)
+
+    def check(case, out, what):
+        cq, ckc, cvc, ct, cl = case
+        assert_decode_close(out, oracle_decode(cq, ckc, cvc, ct, cl, 1 / math.sqrt(hd)), dtype, what=what)
+
+    for i, case in enumerate(cases):          # eager: each call right after the copies
+        load(case)
+        out = step.decode().clone()
+        check(case, out, f"eager case {i}")
+    graphs = []
+    for case in cases:                        # the copies and the call captured together
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            load(case)
+            step.decode()
+        graphs.append(g)
+    for rep in range(2):
+        for i, (case, g) in enumerate(zip(cases, graphs)):
+            g.replay()
+            check(case, step.out.clone(), f"graph case {i}, replay {rep}")
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
