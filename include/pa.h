@@ -52,7 +52,7 @@ extern "C" {
 /* ---- return codes ---------------------------------------------------- */
 #define PA_OK 0
 #define PA_ERR_INVALID_ARG -1 /* null pointer, bad size, inconsistent shape */
-#define PA_ERR_UNSUPPORTED -2 /* valid request this build has no kernel for */
+#define PA_ERR_UNSUPPORTED -2 /* valid request the library has no kernel for */
 #define PA_ERR_CUDA -3        /* a CUDA runtime/driver call failed */
 #define PA_ERR_BAD_INDEX -4   /* host-visible id out of range */
 #define PA_ERR_NO_BLOCKS -5   /* block manager: free pool exhausted */
