@@ -13,7 +13,7 @@ Semantics restated from the pages:
 - ayinedjimi-consultants.fr glossary, "Definition": unused blocks are recycled
   immediately; N sampled candidates share the prompt's blocks until they diverge.
 
-Allocation policy (a choice of this build, stated so the model and the library
+Allocation policy (a choice made here, stated so the model and the library
 can be compared id for id): the free pool is a stack; it starts so that block
 0 is handed out first, then 1, 2, ...; a freed block is pushed on top and is
 the next one handed out; a sequence's blocks are released from its last

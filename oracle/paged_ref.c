@@ -26,7 +26,7 @@
  * softmax taken as exp(s - max s) / sum.  Cache elements are fp32 or bf16
  * (raw bits) and are widened exactly to fp64; q is passed already in fp64.
  *
- * Layouts (row-major, chosen by this build because the pages fix none):
+ * Layouts (row-major, chosen here because the pages fix none):
  *   cache          [num_blocks][num_kv_heads][block_size][head_dim]
  *   q, out         [num_seqs][num_q_heads][head_dim]
  *   block_tables   [num_seqs][max_blocks_per_seq]  int32
