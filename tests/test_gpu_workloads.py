@@ -172,3 +172,27 @@ def test_prefix_cached_batch_decodes_like_private_copies(pa):
     oracle.reshape_and_cache(kn, vn, kc, vc, slots)
     ref = oracle_decode(q, kc, vc, tables, lens, 0.09)
     assert_decode_close(out, ref, torch.bfloat16, what="prefix-cached batch")
+
+
+def test_f32_longest_contexts_stay_within_1e5(pa):
+    """fp32 at the long-context mix's longest length: two sequences of 131072
+    tokens and one of 16, GQA 16/2, head_dim 128, block_size 32, partitions
+    of 512 (256 partials per row merged), fused cache write; every output
+    within 1e-5 of the oracle."""
+    from helpers import make_case
+    binding, engine, _ = pa
+    lens = [131072, 16, 131072]
+    Hq, Hkv, hd, bs = 16, 2, 128, 32
+    q, kc, vc, tables, lens_t = make_case(lens, Hq, Hkv, hd, bs, torch.float32, seed=97, slack=4, nan_tails=False)
+    tab = tables.cpu()
+    slots = torch.tensor([int(tab[i, (n - 1) // bs]) * bs + (n - 1) % bs for i, n in enumerate(lens)],
+                         dtype=torch.int64)
+    g = torch.Generator().manual_seed(98)
+    kn = torch.randn(3, Hkv, hd, generator=g)
+    vn = torch.randn(3, Hkv, hd, generator=g)
+    step = engine.DecodeStep(q, kc, vc, tables, lens_t, 1 / 128 ** 0.5, max(lens), 512)
+    out = step.run_fused(kn.cuda(), vn.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    assert step.status.read() == 0
+    ref = oracle_decode(q, kc, vc, tables, lens_t, 1 / 128 ** 0.5)    # caches already hold the new rows
+    assert_decode_close(out, ref, torch.float32, what="fp32 131072-token sequences")
