@@ -17,17 +17,18 @@ pytestmark = pytest.mark.gpu
 
 
 def bits(t):
-    return t.view(torch.int16)
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
 
 
-def test_multi_step_serving_loop_matches_the_oracle():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_multi_step_serving_loop_matches_the_oracle(dtype):
     from paged_kv_cache_237_gb300 import binding
     from paged_kv_cache_237_gb300.engine import DecodeStep
     rng = np.random.default_rng(17)
     nb, bs, Hq, Hkv, hd, scale = 400, 16, 16, 2, 128, 0.09
     g = torch.Generator().manual_seed(17)
-    kc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(torch.bfloat16)     # arbitrary prompt K/V
-    vc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(torch.bfloat16)
+    kc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(dtype)     # arbitrary prompt K/V
+    vc_h = torch.randn(nb, Hkv, bs, hd, generator=g).to(dtype)
     kc, vc = kc_h.cuda(), vc_h.cuda()
     bm = binding.BlockManager(nb, bs)
     prompts = {t: rng.integers(0, 30000, size=int(rng.integers(300, 700))).tolist() for t in range(2)}
@@ -55,9 +56,9 @@ def test_multi_step_serving_loop_matches_the_oracle():
         seqs = list(live)
         slots, pairs = bm.append_slots(seqs)
         tables, lens = bm.build_tables(seqs, max(len(bm.block_table(s)) for s in seqs))
-        q = torch.randn(len(seqs), Hq, hd, generator=g).to(torch.bfloat16)
-        kn = torch.randn(len(seqs), Hkv, hd, generator=g).to(torch.bfloat16)
-        vn = torch.randn(len(seqs), Hkv, hd, generator=g).to(torch.bfloat16)
+        q = torch.randn(len(seqs), Hq, hd, generator=g).to(dtype)
+        kn = torch.randn(len(seqs), Hkv, hd, generator=g).to(dtype)
+        vn = torch.randn(len(seqs), Hkv, hd, generator=g).to(dtype)
         dstep = DecodeStep(q.cuda(), kc, vc, tables.cuda(), lens.cuda(), scale, int(lens.max()), 64,
                            status=status)
         out = dstep.run_fused(kn.cuda(), vn.cuda(), slots.cuda(), pairs.cuda() if pairs.numel() else None)
@@ -69,7 +70,7 @@ def test_multi_step_serving_loop_matches_the_oracle():
             oracle.copy_blocks(kc_h, vc_h, pairs)
         oracle.reshape_and_cache(kn, vn, kc_h, vc_h, slots)
         ref = oracle.paged_decode(q, kc_h, vc_h, tables, lens, scale)
-        assert_decode_close(out, ref, torch.bfloat16, what=f"serving step {step}")
+        assert_decode_close(out, ref, dtype, what=f"serving step {step} {dtype}")
     assert torch.equal(bits(kc.cpu()), bits(kc_h)) and torch.equal(bits(vc.cpu()), bits(vc_h))
 
 
