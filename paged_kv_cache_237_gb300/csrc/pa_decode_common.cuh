@@ -152,8 +152,8 @@ __device__ __forceinline__ bool next_item(Item &it, SeqCursor &cur, long long it
 
 // Physical location of this warp's k-th chunk of the item, as a row of the
 // [num_blocks * Hkv * block_size, head_dim] view of a cache; an invalid block
-// id gives -1 and sets a flag (the bf16 path then loads rows past the view,
-// which TMA fills with zeros; the fp32 path skips the copy).
+// id gives -1 and sets a flag (the passes then load rows past the view, which
+// TMA fills with zeros).
 template <int NW = kWarps>
 __device__ __forceinline__ int chunk_row(const DecodeParams &p, const Item &it, int warp, int k) {
     const int c = warp + NW * k;
