@@ -399,10 +399,15 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
     // Staged variant (4-warp CTAs, at most kReduceMaxPartsSmall partitions):
     // every partial of the row is copied into shared memory at once (cp.async,
     // no registers held), so the row costs one round trip however many
-    // partitions it has.  Otherwise the partials are read as they are summed.
+    // partitions it has.  Otherwise (8 warps, long rows) the first kHeadParts
+    // partitions of each warp are copied the same way while the maximum is
+    // taken, and the rest are read as they are summed: rows of up to
+    // 8 x kHeadParts partitions also cost one round trip.
     constexpr bool kStaged = kReduceWarps == 4;
+    constexpr int kHeadParts = kStaged ? 1 : 4;
     extern __shared__ float4 s_stage[];            // [max_parts][HD / 4] accumulators, then [max_parts] (m, l)
     float2 *s_ml = reinterpret_cast<float2 *>(s_stage + (kStaged ? p.max_parts * (HD / 4) : 0));
+    __shared__ float4 s_head[kStaged ? 1 : kHeadParts * kReduceWarps][HD / 4];
     if constexpr (kStaged) {
         if (active)
             for (int i = warp; i < np; i += kReduceWarps)
@@ -411,6 +416,15 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
             cp_async_8(smem_addr(s_ml + i), p.part_ml + (base + i * stride) * 2);
         cp_async_wait_all();
         __syncthreads();
+    } else {
+        if (active)
+#pragma unroll
+            for (int j = 0; j < kHeadParts; ++j) {
+                const int i = warp + j * kReduceWarps;
+                if (i < np)
+                    cp_async_16(smem_addr(&s_head[i][lane]), p.part_acc + (base + i * stride) * HD + lane * 4);
+            }
+        cp_async_commit();
     }
     auto ml_of = [&](int i) -> float2 {
         if constexpr (kStaged) return s_ml[i];
@@ -427,6 +441,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
 #pragma unroll
     for (int w = 1; w < kReduceWarps; ++w) M = fmaxf(M, s_max[w]);
 
+    if constexpr (!kStaged) cp_async_wait_group<0>();   // this lane's head partials have landed
+
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
@@ -438,6 +454,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
             float4 v;
             if constexpr (kStaged)
                 v = s_stage[i * (HD / 4) + lane];
+            else if (i < kHeadParts * kReduceWarps)
+                v = s_head[i][lane];                   // copied by this lane, ordered by its own wait
             else
                 v = *reinterpret_cast<const float4 *>(p.part_acc + (base + i * stride) * HD + lane * 4);
             acc.x += f * v.x;
