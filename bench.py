@@ -45,11 +45,11 @@ L2_BYTES = 129 * 2**20
 # seeded slice of the same length mix (--num-seqs), scaled to the full launch
 # by the ratio of algorithmic bytes.  Valid only while the kernel source is
 # the one captured.
-TRAFFIC_CAPTURE = {"source_sha256_prefix": "2764a544014fc5fc",
-                   # 48-sequence slice: 4,143,659,520 B read + 26,297,856 B written
+TRAFFIC_CAPTURE = {"source_sha256_prefix": "d2092055b73d411c",
+                   # 48-sequence slice: 4,143,338,496 B read + 26,150,400 B written
                    # over 4,141,526,704 algorithmic bytes, scaled to 20,791,665,640
-                   "bytes_per_launch": {"long_context": 20934395862,
-                                        "gqa_llama3_70b": 902334976 + 6202112}}
+                   "bytes_per_launch": {"long_context": 20932043957,
+                                        "gqa_llama3_70b": 902361344 + 6061312}}
 
 
 KERNEL_FILES = ("pa_decode.cu", "pa_decode_common.cuh", "pa_internal.h")
